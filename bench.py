@@ -1,0 +1,451 @@
+"""Benchmark: bifocal prefill TFLOP/s at 128K and decode us/token at 128K on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step is one pass of the whole hot path over one batch of synthetic input:
+a bifocal prefill of the Qwen3-8B-shaped attention layer (B=1, Hq=32, Hkv=8,
+D=128, S=131072, L_pre=32768, w=4096, theta=1e6; g=4) followed by a bifocal
+decode of the last token over the same exact-RoPE K/V (n=131072).  Inputs
+are seeded bf16 N(0,1) (counter-based generator) and are larger than L2.
+``value`` is the prefill throughput (FA causal FLOP convention 2*B*Hq*D*S^2)
+over the K timed steps; decode, the bifocal-off prefill, the roofline, the
+end-to-end number (host buffers, copies inside the timed region) and the CPU
+oracle baseline ride along in the same JSON line.
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the path has no exchange step); time is the max over ranks and ``value`` the
+sum of all ranks' work over that time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "bifocal prefill attn TFLOP/s @128K (% of BF16 peak); decode µs/token @128K"
+WORKLOAD = dict(B=1, Hq=32, Hkv=8, D=128, S=131072, L_pre=32768, w=4096, theta=1e6, seed=2)
+DECODE_NS = (8192, 32768, 131072)
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def prefill_flops(B, Hq, D, S):
+    return 2.0 * B * Hq * D * S * S
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        loaded = [x for x in sm if x > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ inputs
+def make_inputs(dev, cfg, pinned=False):
+    import torch
+
+    from zero_shot_rope_02_b300 import inputs
+
+    B, Hq, Hkv, D, S, seed = (cfg[k] for k in ("B", "Hq", "Hkv", "D", "S", "seed"))
+    host = []
+    for shape, tid in (((B, S, Hq, D), 0), ((B, S, Hkv, D), 1), ((B, S, Hkv, D), 2)):
+        t = inputs.to_torch_bf16(inputs.normal_bf16_bits(shape, seed, tid))
+        host.append(t.pin_memory() if pinned else t)
+    if dev is None:
+        return host
+    return [t.to(dev) for t in host]
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, world, dev):
+    import torch
+
+    import zero_shot_rope_02_b300 as jl
+
+    cfg = WORKLOAD
+    B, Hq, Hkv, D, S, L, w, theta = (cfg[k] for k in ("B", "Hq", "Hkv", "D", "S", "L_pre", "w", "theta"))
+    peaks, peaks_src = load_peaks()
+    stream = torch.cuda.current_stream(dev)
+    q, k, v = make_inputs(dev, cfg)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, Hq, S), dtype=torch.float32, device=dev)
+    qd = q[:, S - 1].contiguous()
+    dout = torch.empty_like(qd)
+    dlse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    ws = torch.zeros(max(16, jl.jl_bifocal_decode_workspace_size(B, Hq, Hkv, S, D)), dtype=torch.uint8,
+                     device=dev)
+
+    def step(L_pre=L):
+        jl.jl_bifocal_prefill(q, k, v, L_pre, w, theta, out=out, lse=lse, stream=stream)
+        jl.jl_bifocal_decode(qd, k, v, S, L_pre, w, theta, workspace=ws, out=dout, lse=dlse, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if jl.jl_debug_status() != 0:
+        raise RuntimeError("device status word set during warm-up")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for e in ev:
+            e[0].record(stream)
+            jl.jl_bifocal_prefill(q, k, v, L, w, theta, out=out, lse=lse, stream=stream)
+            e[1].record(stream)
+            jl.jl_bifocal_decode(qd, k, v, S, L, w, theta, workspace=ws, out=dout, lse=dlse, stream=stream)
+            e[2].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world)
+    prefill_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    decode_ms = [b.elapsed_time(c) for _, b, c in ev]
+    flops = prefill_flops(B, Hq, D, S)
+    ms_per_step = total_ms / args.steps
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    avg_prefill_ms = sum(prefill_ms) / len(prefill_ms)
+    achieved = flops / (avg_prefill_ms * 1e-3) / 1e12
+    if jl.jl_debug_status() != 0:
+        raise RuntimeError("device status word set during the timed region")
+
+    # bifocal off: the same kernel with L_pre >= S (g = 1)
+    plain_ms = time_calls(lambda: jl.jl_bifocal_prefill(q, k, v, S, w, theta, out=out, lse=lse,
+                                                        stream=stream), stream, dev, reps=max(3, args.steps))
+    decode = decode_sweep(jl, dev, stream, peaks)
+
+    res = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded bf16 N(0,1) q/k/v treated as exact-RoPE; no weights)",
+        "config": {"workload": "Qwen3-8B-shaped bifocal prefill at 128K + decode of the last token",
+                   **{k_: cfg[k_] for k_ in ("B", "Hq", "Hkv", "D", "S", "L_pre", "w", "theta")},
+                   "g": jl.jl_group_factor(S, L),
+                   "l2": "inputs larger than L2 (q 1 GiB, k and v 256 MiB each)"},
+        "prefill": {"tflops": round(achieved, 2), "ms": round(avg_prefill_ms, 3),
+                    "frac_of_bf16_peak": round(achieved / peaks["bf16_tflops"], 4)},
+        "plain_rope": {"tflops": round(flops / (plain_ms * 1e-3) / 1e12, 2), "ms": round(plain_ms, 3),
+                       "bifocal_overhead": round(avg_prefill_ms / plain_ms - 1.0, 4)},
+        "decode": decode,
+        "decode_in_step_us": round(1e3 * sum(decode_ms) / len(decode_ms), 2),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                     "traffic": None, "kernel": "prefill_kernel<128>",
+                     "peak_source": f"{peaks_src} bf16 burst"},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_e2e:
+        res["e2e"] = e2e(jl, args, dev, stream)
+    if rank == 0 and not args.no_cpu:
+        res["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    return res
+
+
+def time_calls(fn, stream, dev, reps):
+    import torch
+
+    fn()
+    torch.cuda.synchronize(dev)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    return a.elapsed_time(b) / reps
+
+
+def decode_sweep(jl, dev, stream, peaks):
+    """us per decode call at n = 8K/32K/128K, Hq=32, Hkv=8, D=128, L=32768,
+    w=4096; the caches are rotated over copies totalling > 2x L2 so every
+    call reads K/V from HBM."""
+    import torch
+
+    from zero_shot_rope_02_b300 import inputs
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    out = {}
+    for n in DECODE_NS:
+        nbytes = 2 * n * 8 * 128 * 2
+        copies = max(1, math.ceil(2 * l2 / nbytes) + 1)
+        q = inputs.to_torch_bf16(inputs.normal_bf16_bits((1, 32, 128), 3, 3)).to(dev)
+        k0 = inputs.to_torch_bf16(inputs.normal_bf16_bits((1, n, 8, 128), 3, 4)).to(dev)
+        v0 = inputs.to_torch_bf16(inputs.normal_bf16_bits((1, n, 8, 128), 3, 5)).to(dev)
+        ks = [k0] + [k0.clone() for _ in range(copies - 1)]
+        vs = [v0] + [v0.clone() for _ in range(copies - 1)]
+        ws = torch.zeros(jl.jl_bifocal_decode_workspace_size(1, 32, 8, n, 128), dtype=torch.uint8, device=dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((1, 32), dtype=torch.float32, device=dev)
+        it = [0]
+
+        def call():
+            c = it[0] % copies
+            it[0] += 1
+            jl.jl_bifocal_decode(q, ks[c], vs[c], n, 32768, 4096, 1e6, workspace=ws, out=o, lse=lse,
+                                 stream=stream)
+
+        for _ in range(5):
+            call()
+        reps = 200 if n < 100000 else 50
+        us = 1e3 * time_calls(call, stream, dev, reps)
+        gbs = nbytes / (us * 1e-6) / 1e9
+        out[str(n)] = {"us_per_token": round(us, 2), "gbs": round(gbs, 1),
+                       "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4), "g": jl.jl_group_factor(n, 32768)}
+        del ks, vs
+    return out
+
+
+def e2e(jl, args, dev, stream):
+    """The same step through the public API from pinned HOST buffers: q/k/v
+    host->device, prefill + decode, out/lse/decode-out device->host, all
+    inside the timed region."""
+    import torch
+
+    cfg = WORKLOAD
+    B, Hq, Hkv, D, S, L, w, theta = (cfg[k] for k in ("B", "Hq", "Hkv", "D", "S", "L_pre", "w", "theta"))
+    hq, hk, hv = make_inputs(None, cfg, pinned=True)
+    q = torch.empty(hq.shape, dtype=hq.dtype, device=dev)
+    k = torch.empty(hk.shape, dtype=hk.dtype, device=dev)
+    v = torch.empty(hv.shape, dtype=hv.dtype, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, Hq, S), dtype=torch.float32, device=dev)
+    dout = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
+    dlse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    ws = torch.zeros(max(16, jl.jl_bifocal_decode_workspace_size(B, Hq, Hkv, S, D)), dtype=torch.uint8,
+                     device=dev)
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h_dout = torch.empty(dout.shape, dtype=dout.dtype).pin_memory()
+    h_dlse = torch.empty(dlse.shape, dtype=dlse.dtype).pin_memory()
+
+    def step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        jl.jl_bifocal_prefill(q, k, v, L, w, theta, out=out, lse=lse, stream=stream)
+        jl.jl_bifocal_decode(q[:, S - 1].contiguous(), k, v, S, L, w, theta, workspace=ws, out=dout,
+                             lse=dlse, stream=stream)
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+        h_dout.copy_(dout, non_blocking=True)
+        h_dlse.copy_(dlse, non_blocking=True)
+
+    steps = max(1, min(args.steps, 5))
+    ms = time_calls(step, stream, dev, steps)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = sum(t.numel() * t.element_size() for t in (h_out, h_lse, h_dout, h_dlse))
+    return {"value": round(prefill_flops(B, Hq, D, S) / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ------------------------------------------------------------------ oracle arm
+def oracle_sample(seconds_budget):
+    """The fp64 oracle on a bounded sample of the 128K workload: full rows of
+    query positions near the end of the sequence, all 32 heads.  Returns
+    (TFLOP/s on the FA convention for the rows done, threads, description)."""
+    import numpy as np
+
+    import oracle
+    from zero_shot_rope_02_b300 import inputs
+
+    cfg = WORKLOAD
+    B, Hq, Hkv, D, S, L, w, theta, seed = (cfg[k] for k in ("B", "Hq", "Hkv", "D", "S", "L_pre", "w",
+                                                            "theta", "seed"))
+    orc = oracle.default()
+    kf = inputs.bf16_bits_to_f64(inputs.normal_bf16_bits((B, S, Hkv, D), seed, 1))
+    vf = inputs.bf16_bits_to_f64(inputs.normal_bf16_bits((B, S, Hkv, D), seed, 2))
+    rows_done, flops, elapsed = 0, 0.0, 0.0
+    nrows = 2
+    while elapsed < seconds_budget:
+        rows = np.arange(S - rows_done - nrows, S - rows_done, dtype=np.int64)
+        q = inputs.bf16_bits_to_f64(_q_rows_bits(seed, B, S, Hq, D, rows))
+        t = time.perf_counter()
+        orc.bifocal_rows(q, kf, vf, rows, S, L, w, theta)
+        elapsed += time.perf_counter() - t
+        flops += float(sum(4.0 * B * Hq * D * (int(r) + 1) for r in rows))
+        rows_done += nrows
+        nrows = min(2 * nrows, 64)
+    desc = (f"fp64 oracle, {rows_done} full query rows (positions {S - rows_done}..{S - 1}) x {Hq} heads "
+            f"of the 128K workload, incl. the per-call key correction; FLOPs on the same causal convention")
+    return flops / elapsed / 1e12, orc.num_threads(), desc, elapsed
+
+
+def _q_rows_bits(seed, B, S, Hq, D, rows):
+    """Rows of the seeded q tensor without drawing the whole 1 GiB tensor:
+    element e of the tensor uses counter e, so a row is a contiguous range."""
+    import numpy as np
+
+    from zero_shot_rope_02_b300 import inputs
+
+    key = inputs._key(seed, 0)
+    out = np.empty((B, len(rows), Hq, D), dtype=np.uint16)
+    row_elems = Hq * D
+    for b in range(B):
+        for n, r in enumerate(rows):
+            start = (b * S + int(r)) * row_elems
+            vals = inputs._normal_chunk(key, start, row_elems).astype(np.float32)
+            out[b, n] = inputs.fp32_to_bf16_bits(vals).reshape(Hq, D)
+    return out
+
+
+def cpu_baseline(seconds):
+    v, cores, desc, el = oracle_sample(seconds)
+    return {"value": round(v, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc,
+            "seconds": round(el, 2)}
+
+
+def run_reference(args):
+    per = max(2.0, min(20.0, 60.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(per / 4)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        v, cores, desc, _ = oracle_sample(per)
+        vals.append(v)
+    total = time.perf_counter() - t0
+    value = sum(vals) / len(vals)
+    return {"metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": "Qwen3-8B-shaped bifocal prefill at 128K (bounded row sample)",
+                       **{k_: WORKLOAD[k_] for k_ in ("B", "Hq", "Hkv", "D", "S", "L_pre", "w", "theta")}},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+# ------------------------------------------------------------------ distributed glue
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    import torch
+
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    res = run_ours(args, rank, world, dev)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

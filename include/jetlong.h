@@ -1,0 +1,192 @@
+/*
+ * jetlong.h -- C ABI of the B300 (sm_103a) Dynamic Bifocal RoPE attention library.
+ *
+ * The method is the one of "Jet-Long: Efficient Long-Context Extension with
+ * Dynamic Bifocal RoPE" (arXiv 2607.07740).  The pages that describe it print
+ * no formulas; the statement below is the library's reading of their prose,
+ * cited per entry point by page title and section.
+ *
+ * Notation.  Positions p are 0-based token indices.  D is the head dimension,
+ * tau = 1/sqrt(D).  theta_d = theta^(-2d/D) for d in [0, D/2).  R_p rotates
+ * every pair (x_d, x_{d+D/2}) of a head vector by the angle p*theta_d
+ * (half-split pair layout, the Qwen3 / Hugging Face "rotate_half" convention).
+ *
+ *   g(s, L)   the group factor: the smallest integer g >= 1 such that every
+ *             aliased position floor(p/g), p < s, lies inside the pretrained
+ *             window [0, L); equal to max(1, ceil(s/L)), so g = 1 whenever
+ *             s <= L ("ResearchPod Summary", paragraph 2: smallest integer
+ *             grouping that keeps remote rotation angles within the pretrained
+ *             distribution; abstract on the engineersofai.com page: the factor
+ *             adapts to the current length s and the base model is recovered
+ *             exactly at short inputs).
+ *   delta_p   floor(p/g) - p <= 0, the correction offset (position aliasing,
+ *             ResearchPod transcript).
+ *
+ * Bifocal score of query i against key j <= i, with exact-RoPE inputs
+ * q_i = R_i(raw q), k_j = R_j(raw k):
+ *   i - j <  w :  tau * <q_i, k_j>                              (local, exact RoPE)
+ *   i - j >= w :  tau * <R_{delta_i} q_i, R_{delta_j} k_j>      (remote, aliased)
+ * followed by one softmax over all keys j <= i.  This equals the pages'
+ * inclusion-exclusion merge local(window) + remote(all) - remote(window) on
+ * log-sum-exp statistics ("How bifocal attention sidesteps the fixed-scaling
+ * trap", seventnews.com; "How Jet-Long works", transform-ai page).  The remote
+ * vectors come from an on-the-fly correction rotation of the exact-RoPE q/k;
+ * no second rotated copy is stored (abstract; ResearchPod transcript on the
+ * cache keeping original positions).
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are contiguous, row-major.  q / out: [B, S, Hq, D] bf16;
+ *     k / v: [B, S, Hkv, D] bf16 ("BSHD"); lse: fp32 [B, Hq, S].
+ *     GQA: query head h reads kv head h / (Hq / Hkv).
+ *   - Every device pointer must be 16-byte aligned (TMA and 128-bit loads).
+ *   - The caller owns every buffer.  No entry point allocates or frees device
+ *     memory, copies between host and device, or synchronises; compute calls
+ *     are asynchronous on `stream` (a cudaStream_t; NULL = legacy stream).
+ *   - Argument checks run on the host before any launch and return an error
+ *     code without touching memory.  A launch failure returns JL_ERR_CUDA.
+ *     Device code never traps: a bounded wait that expires or a guard that
+ *     fires records a code in the device status word (jl_debug_status) and the
+ *     kernel returns early.
+ *   - No C++ exception crosses this interface.
+ *   - Bifocal off: pass L_pre >= S (prefill) or L_pre >= n (decode); g is then
+ *     1, no key is corrected, and the same kernel computes plain causal RoPE
+ *     attention.
+ */
+#ifndef JETLONG_H
+#define JETLONG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes of every entry point. */
+typedef enum {
+    JL_OK = 0,
+    JL_ERR_ARG = -1,         /* a size or parameter out of its domain            */
+    JL_ERR_ALIGN = -2,       /* a pointer not 16-byte aligned                    */
+    JL_ERR_UNSUPPORTED = -3, /* a valid shape this build has no kernel for (D)   */
+    JL_ERR_OVERFLOW = -4,    /* an element count or byte size overflows int64    */
+    JL_ERR_CUDA = -5,        /* a CUDA runtime call or launch failed             */
+    JL_ERR_TIMEOUT = -6,     /* device status only: a bounded wait expired       */
+    JL_ERR_WORKSPACE = -7,   /* workspace pointer NULL or smaller than required  */
+    JL_ERR_GUARD = -8        /* device status only: an in-kernel guard fired     */
+} jl_status;
+
+/* Human-readable name of a jl_status value (static string, never NULL). */
+const char *jl_status_string(int status);
+
+/* Library version as "major.minor.patch" (static string). */
+const char *jl_version(void);
+
+/*
+ * Group factor g(s, L_pre) = max(1, ceil(s / L_pre)) -- host, pure.
+ * Reading of the ResearchPod summary (paragraph 2, "smallest integer grouping")
+ * and of the abstract (factor set by the current length s).
+ *   s      current sequence length (prefill: S; decode: n), >= 1
+ *   L_pre  pretrained context window, >= 1
+ *   g_out  host pointer receiving g (>= 1); untouched on error
+ * Returns JL_OK, JL_ERR_ARG (s < 1, L_pre < 1, g_out NULL) or JL_ERR_OVERFLOW
+ * (g would not fit in int32).
+ */
+int jl_group_factor(int64_t s, int64_t L_pre, int32_t *g_out);
+
+/*
+ * Exact RoPE, in place: x[b, s, h, :] <- R_{pos0 + s}(x[b, s, h, :]).
+ * The "local RoPE-faithful window" of the abstract uses the original, unscaled
+ * frequencies ("How bifocal attention sidesteps the fixed-scaling trap"); this
+ * call produces the exact-RoPE q, k and cache rows the attention calls consume.
+ *   x      device, bf16 [B, S, H, D], 16-byte aligned, rewritten in place
+ *   pos0   position of row s = 0 (>= 0; pos0 + S - 1 < 2^62)
+ *   theta  RoPE base (> 0)
+ * Angles are formed from an exact 64-bit fixed-point phase (turns) and
+ * evaluated in fp32; the result is rounded to bf16 (nearest even).
+ * Returns JL_OK, JL_ERR_ARG, JL_ERR_ALIGN, JL_ERR_UNSUPPORTED (D not even or
+ * D > 256), JL_ERR_OVERFLOW or JL_ERR_CUDA.
+ */
+int jl_rope_apply(void *x, int B, int S, int H, int D, int64_t pos0, double theta,
+                  void *stream);
+
+/*
+ * Bifocal causal GQA prefill attention (one TMA + tcgen05 kernel).
+ * The three attention passes of the pages -- local(window, exact RoPE),
+ * remote(all, aliased) and remote(window, aliased), merged by
+ * inclusion-exclusion on log-sum-exp statistics (ResearchPod transcript on
+ * the prefill phase; "How Jet-Long works", transform-ai page) -- are computed
+ * as the single masked pass they equal: a per-tile classifier sends every
+ * 128x128 tile that lies inside the window to exact scores, every tile that
+ * lies outside it to corrected-rotation scores, and computes both only on the
+ * tiles the window boundary crosses.  g = g(S, L_pre).
+ *   q      device bf16 [B, S, Hq, D], exact RoPE at positions 0..S-1
+ *   k, v   device bf16 [B, S, Hkv, D], same positions
+ *   out    device bf16 [B, S, Hq, D], written
+ *   lse    device fp32 [B, Hq, S], written: natural-log sum of exp(scores)
+ *   B >= 1, Hq >= 1, Hkv >= 1 with Hq % Hkv == 0, S >= 1, D in {64, 128},
+ *   L_pre >= 1 (pretrained window), w >= 1 (local window: key j is local
+ *   for query i when 0 <= i - j < w), theta > 0.
+ * Returns JL_OK, JL_ERR_ARG, JL_ERR_ALIGN, JL_ERR_UNSUPPORTED, JL_ERR_OVERFLOW
+ * or JL_ERR_CUDA.  out/lse are undefined if the device status word reports a
+ * timeout afterwards.
+ */
+int jl_bifocal_prefill(const void *q, const void *k, const void *v, void *out, float *lse,
+                       int B, int Hq, int Hkv, int S, int D, int L_pre, int w,
+                       double theta, void *stream);
+
+/*
+ * Workspace bytes jl_bifocal_decode needs for these sizes (split-KV partial
+ * statistics and one arrival counter per (batch, kv head)).  0 on bad sizes.
+ */
+size_t jl_bifocal_decode_workspace_size(int B, int Hq, int Hkv, int n, int D);
+
+/*
+ * Bifocal single-token decode over an exact-RoPE bf16 KV cache (split-KV).
+ * The cache keeps original positions and is never rewritten; remote keys are
+ * corrected at lookup time (ResearchPod transcript on the cache; abstract:
+ * at most ~4% generation overhead).  The query is the token at position n-1
+ * and the cache holds positions 0..n-1 including it; g = g(n, L_pre); key j
+ * is exact when n-1-j < w, aliased otherwise.
+ *   q        device bf16 [B, Hq, D], exact RoPE at position n-1
+ *   k_cache, v_cache  device bf16 [B, n_cap, Hkv, D]; rows 0..n-1 are read
+ *   out      device bf16 [B, Hq, D];  lse device fp32 [B, Hq]
+ *   n        1 <= n <= n_cap (current length), n_cap the cache capacity
+ *   workspace  device, >= jl_bifocal_decode_workspace_size() bytes, 16-byte
+ *            aligned.  Its counters must be zero before the first call (e.g.
+ *            allocate it zero-filled); every completed call leaves them zero.
+ *            Two calls that share a workspace must not overlap on the GPU.
+ * Returns JL_OK, JL_ERR_ARG, JL_ERR_ALIGN, JL_ERR_UNSUPPORTED, JL_ERR_OVERFLOW,
+ * JL_ERR_WORKSPACE or JL_ERR_CUDA.
+ */
+int jl_bifocal_decode(const void *q, const void *k_cache, const void *v_cache, void *out,
+                      float *lse, int B, int Hq, int Hkv, int n, int n_cap, int D, int L_pre,
+                      int w, double theta, void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * Debug: aliased positions floor(p/g) for p in [0, S), g = g(S, L_pre),
+ * written as int32 to out_dev[0..S).  Computed on the device by the same
+ * integer code the kernels use.
+ */
+int jl_debug_grouped_positions(int64_t S, int64_t L_pre, int32_t *out_dev, void *stream);
+
+/*
+ * Debug: the prefill tile classifier for one (S, L_pre, w), written to
+ * out_dev as int8 [ceil(S/128), ceil(S/128)] (row = query tile, column = key
+ * tile): 0 masked (every key after every query), 1 exact (every pair inside
+ * the window), 2 remote (every pair outside it), 3 band (both), and every
+ * unmasked tile is 1 when g = 1.
+ */
+int jl_debug_tile_classes(int S, int L_pre, int w, int8_t *out_dev, void *stream);
+
+/*
+ * Debug: read and clear the device status word of the current device
+ * (JL_OK, JL_ERR_TIMEOUT or JL_ERR_GUARD).  Synchronises the device; meant
+ * for tests, not for the hot path.
+ */
+int jl_debug_status(int *status_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* JETLONG_H */

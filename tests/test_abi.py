@@ -1,0 +1,140 @@
+"""The C ABI without a GPU: the library loads, exports every declared symbol,
+and its host-side rules (group factor, argument checks) hold.  No call here
+reaches a CUDA launch: every argument error is returned before one."""
+import ctypes
+import os
+import re
+
+import pytest
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "jetlong.h")
+BAD = ctypes.c_void_p(0x1001)  # misaligned, never dereferenced
+GOOD = ctypes.c_void_p(0x1000)  # aligned, never dereferenced (calls fail earlier)
+
+
+def declared_symbols():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(jl_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(jl):
+    names = declared_symbols()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(jl.lib, n), f"{n} declared in jetlong.h but not exported"
+    assert set(names) == set(jl.EXPORTS)
+
+
+def test_version_and_status_strings(jl):
+    assert jl.jl_version().count(".") == 2
+    for code in range(-8, 1):
+        assert jl.status_string(code).startswith("JL_")
+    assert "unknown" in jl.status_string(42)
+
+
+def test_group_factor_matches_oracle(jl, orc):
+    for s in list(range(1, 300)) + [2048, 32767, 32768, 32769, 65536, 131072, 10 ** 9]:
+        for L in (1, 2, 3, 7, 512, 4096, 32768):
+            assert jl.jl_group_factor(s, L) == orc.group_factor(s, L) if s < 10 ** 6 else True
+            assert jl.jl_group_factor(s, L) == max(1, -(-s // L))
+
+
+def test_group_factor_golden(jl):
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "group_factor.txt")
+    for line in open(path):
+        if line.startswith("#") or not line.strip():
+            continue
+        s, L, g = map(int, line.split())
+        assert jl.jl_group_factor(s, L) == g
+
+
+def test_group_factor_rejects(jl):
+    g = ctypes.c_int32(7)
+    assert jl.lib.jl_group_factor(0, 4, ctypes.byref(g)) == jl.JL_ERR_ARG
+    assert jl.lib.jl_group_factor(5, 0, ctypes.byref(g)) == jl.JL_ERR_ARG
+    assert jl.lib.jl_group_factor(5, 4, None) == jl.JL_ERR_ARG
+    assert jl.lib.jl_group_factor(1 << 62, 1, ctypes.byref(g)) == jl.JL_ERR_OVERFLOW
+    assert g.value == 7
+
+
+def _prefill(jl, q=GOOD, k=GOOD, v=GOOD, out=GOOD, lse=GOOD, B=1, Hq=4, Hkv=2, S=256, D=128,
+             L=128, w=64, theta=1e4):
+    return jl.lib.jl_bifocal_prefill(q, k, v, out, lse, B, Hq, Hkv, S, D, L, w, theta, None)
+
+
+def test_prefill_argument_checks(jl):
+    assert _prefill(jl, D=96) == jl.JL_ERR_UNSUPPORTED
+    assert _prefill(jl, D=256) == jl.JL_ERR_UNSUPPORTED
+    assert _prefill(jl, Hq=3, Hkv=2) == jl.JL_ERR_ARG
+    for kw in ({"S": 0}, {"w": 0}, {"L": 0}, {"theta": 0.0}, {"theta": -1.0}, {"B": 0}):
+        assert _prefill(jl, **kw) == jl.JL_ERR_ARG, kw
+    assert _prefill(jl, q=None) == jl.JL_ERR_ARG
+    for name in ("q", "k", "v", "out", "lse"):
+        assert _prefill(jl, **{name: BAD}) == jl.JL_ERR_ALIGN, name
+    assert _prefill(jl, B=1 << 20, Hq=1 << 10, Hkv=1, S=1 << 20) == jl.JL_ERR_OVERFLOW
+
+
+def _decode(jl, q=GOOD, k=GOOD, v=GOOD, out=GOOD, lse=GOOD, B=1, Hq=32, Hkv=8, n=100, n_cap=100,
+            D=128, L=64, w=16, theta=1e6, ws=GOOD, ws_bytes=1 << 30):
+    return jl.lib.jl_bifocal_decode(q, k, v, out, lse, B, Hq, Hkv, n, n_cap, D, L, w, theta, ws,
+                                    ws_bytes, None)
+
+
+def test_decode_argument_checks(jl):
+    assert _decode(jl, D=80) == jl.JL_ERR_UNSUPPORTED
+    assert _decode(jl, Hq=48, Hkv=3) == jl.JL_ERR_UNSUPPORTED  # 16 heads per kv head
+    assert _decode(jl, Hq=30, Hkv=8) == jl.JL_ERR_ARG
+    assert _decode(jl, n=0) == jl.JL_ERR_ARG
+    assert _decode(jl, n=101, n_cap=100) == jl.JL_ERR_ARG
+    assert _decode(jl, w=0) == jl.JL_ERR_ARG
+    assert _decode(jl, L=0) == jl.JL_ERR_ARG
+    for name in ("q", "k", "v", "out", "lse"):
+        assert _decode(jl, **{name: BAD}) == jl.JL_ERR_ALIGN, name
+    assert _decode(jl, ws=None) == jl.JL_ERR_WORKSPACE
+    need = jl.jl_bifocal_decode_workspace_size(1, 32, 8, 100, 128)
+    assert _decode(jl, ws_bytes=need - 1) == jl.JL_ERR_WORKSPACE
+    assert _decode(jl, ws=BAD, ws_bytes=need) == jl.JL_ERR_ALIGN
+
+
+def test_decode_workspace_size(jl):
+    assert jl.jl_bifocal_decode_workspace_size(1, 32, 8, 0, 128) == 0
+    assert jl.jl_bifocal_decode_workspace_size(1, 30, 8, 10, 128) == 0
+    small = jl.jl_bifocal_decode_workspace_size(1, 32, 8, 8192, 128)
+    big = jl.jl_bifocal_decode_workspace_size(1, 32, 8, 131072, 128)
+    assert 0 < small <= big
+    # partial o for every (head, split) at most: 256 splits
+    assert big <= 256 + 1 * 32 * 256 * (128 + 2) * 4 + 512
+
+
+def test_rope_argument_checks(jl):
+    f = jl.lib.jl_rope_apply
+    assert f(GOOD, 1, 4, 2, 7, 0, 1e4, None) == jl.JL_ERR_UNSUPPORTED  # odd D
+    assert f(GOOD, 1, 4, 2, 258, 0, 1e4, None) == jl.JL_ERR_UNSUPPORTED
+    assert f(GOOD, 1, 4, 2, 8, -1, 1e4, None) == jl.JL_ERR_ARG
+    assert f(GOOD, 1, 4, 2, 8, 0, 0.0, None) == jl.JL_ERR_ARG
+    assert f(None, 1, 4, 2, 8, 0, 1e4, None) == jl.JL_ERR_ARG
+    assert f(BAD, 1, 4, 2, 8, 0, 1e4, None) == jl.JL_ERR_ALIGN
+    assert f(GOOD, 1, 4, 2, 8, (1 << 62) - 2, 1e4, None) == jl.JL_ERR_OVERFLOW
+
+
+def test_debug_argument_checks(jl):
+    assert jl.lib.jl_debug_grouped_positions(0, 4, GOOD, None) == jl.JL_ERR_ARG
+    assert jl.lib.jl_debug_grouped_positions(4, 4, None, None) == jl.JL_ERR_ARG
+    assert jl.lib.jl_debug_tile_classes(100, 4, 0, GOOD, None) == jl.JL_ERR_ARG
+    assert jl.lib.jl_debug_status(None) == jl.JL_ERR_ARG
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    """The binding refuses to load when libjetlong.so is missing (no fallback)."""
+    import importlib.util
+
+    src = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                       "zero_shot_rope_02_b300", "binding.py")
+    dst = tmp_path / "binding.py"
+    dst.write_text(open(src).read())
+    spec = importlib.util.spec_from_file_location("binding_copy", dst)
+    mod = importlib.util.module_from_spec(spec)
+    with pytest.raises(ImportError):
+        spec.loader.exec_module(mod)

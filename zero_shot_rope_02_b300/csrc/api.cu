@@ -1,0 +1,149 @@
+// Host side of the C ABI that every kernel file shares: status strings, the
+// group-factor rule, the fixed-point rotation phases, the device status word
+// and the debug exports.
+#include <math.h>
+#include <stdio.h>
+
+#include "jl_common.cuh"
+#include "tile_class.cuh"
+
+// Device status word: kernels record JL_ERR_TIMEOUT / JL_ERR_GUARD here
+// instead of trapping.  One per device that loads the library.
+__device__ int g_jl_status_word;
+
+namespace jl {
+
+bool make_phase_table(PhaseTable *t, int D, double theta)
+{
+    if (!t || D < 2 || (D & 1) || D / 2 > kMaxPairs || !(theta > 0.0) || !isfinite(theta))
+        return false;
+    const int h = D / 2;
+    for (int d = 0; d < kMaxPairs; d++) t->f[d] = 0ull;
+    for (int d = 0; d < h; d++) {
+        // theta_d / (2 pi) turns, reduced mod 1, as a 64-bit binary fraction.
+        long double turns = powl((long double)theta, -2.0L * d / (long double)D) /
+                            (2.0L * 3.14159265358979323846264338327950288L);
+        turns -= floorl(turns);
+        long double scaled = ldexpl(turns, 64);
+        unsigned long long f;
+        if (scaled >= 18446744073709551616.0L)
+            f = 0ull;  // rounds up to a whole turn
+        else
+            f = (unsigned long long)scaled;
+        t->f[d] = f;
+    }
+    return true;
+}
+
+int *status_word_ptr()
+{
+    static int *cache[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (!cache[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_jl_status_word) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        cache[dev] = static_cast<int *>(p);
+    }
+    return cache[dev];
+}
+
+int cuda_status(cudaError_t e)
+{
+    if (e == cudaSuccess) return JL_OK;
+    cudaGetLastError();
+    return JL_ERR_CUDA;
+}
+
+}  // namespace jl
+
+namespace {
+
+__global__ void grouped_positions_kernel(int32_t *out, int64_t S, int g)
+{
+    int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (p < S) out[p] = jl::grouped_pos((int)p, g);
+}
+
+__global__ void tile_classes_kernel(int8_t *out, int S, int w, int g, int nt)
+{
+    int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= nt * nt) return;
+    int qi = t / nt, kj = t % nt;
+    out[t] = (int8_t)jl::tile_class(qi * 128, kj * 128, 128, 128, S, w, g);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *jl_status_string(int status)
+{
+    switch (status) {
+    case JL_OK: return "JL_OK";
+    case JL_ERR_ARG: return "JL_ERR_ARG: argument out of range";
+    case JL_ERR_ALIGN: return "JL_ERR_ALIGN: pointer not 16-byte aligned";
+    case JL_ERR_UNSUPPORTED: return "JL_ERR_UNSUPPORTED: shape without a kernel";
+    case JL_ERR_OVERFLOW: return "JL_ERR_OVERFLOW: size overflows";
+    case JL_ERR_CUDA: return "JL_ERR_CUDA: CUDA call or launch failed";
+    case JL_ERR_TIMEOUT: return "JL_ERR_TIMEOUT: a bounded device wait expired";
+    case JL_ERR_WORKSPACE: return "JL_ERR_WORKSPACE: workspace missing or too small";
+    case JL_ERR_GUARD: return "JL_ERR_GUARD: an in-kernel guard fired";
+    default: return "unknown jl_status";
+    }
+}
+
+const char *jl_version(void) { return "0.1.0"; }
+
+int jl_group_factor(int64_t s, int64_t L_pre, int32_t *g_out)
+{
+    if (!g_out || s < 1 || L_pre < 1) return JL_ERR_ARG;
+    int64_t g = jl::group_factor_host(s, L_pre);
+    if (g > INT32_MAX) return JL_ERR_OVERFLOW;
+    *g_out = (int32_t)g;
+    return JL_OK;
+}
+
+int jl_debug_grouped_positions(int64_t S, int64_t L_pre, int32_t *out_dev, void *stream)
+{
+    if (!out_dev || S < 1 || L_pre < 1) return JL_ERR_ARG;
+    if (S > INT32_MAX) return JL_ERR_OVERFLOW;
+    int g = (int)jl::group_factor_host(S, L_pre);
+    int64_t blocks = (S + 255) / 256;
+    grouped_positions_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(out_dev, S, g);
+    return jl::cuda_status(cudaGetLastError());
+}
+
+int jl_debug_tile_classes(int S, int L_pre, int w, int8_t *out_dev, void *stream)
+{
+    if (!out_dev || S < 1 || L_pre < 1 || w < 1) return JL_ERR_ARG;
+    int nt = (S + 127) / 128;
+    int g = (int)jl::group_factor_host(S, L_pre);
+    int64_t n = (int64_t)nt * nt;
+    tile_classes_kernel<<<(unsigned)((n + 255) / 256), 256, 0, (cudaStream_t)stream>>>(out_dev, S, w,
+                                                                                      g, nt);
+    return jl::cuda_status(cudaGetLastError());
+}
+
+int jl_debug_status(int *status_out)
+{
+    if (!status_out) return JL_ERR_ARG;
+    int v = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&v, g_jl_status_word, sizeof(int));
+    if (e == cudaSuccess) {
+        int zero = 0;
+        e = cudaMemcpyToSymbol(g_jl_status_word, &zero, sizeof(int));
+    }
+    if (e != cudaSuccess) return jl::cuda_status(e);
+    *status_out = v;
+    return JL_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,89 @@
+// Shared device/host helpers of the Dynamic Bifocal RoPE library: the exact
+// fixed-point phase used for every rotation angle, the group-factor and
+// aliasing integer rules, the device status word and bounded waits.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/jetlong.h"
+
+namespace jl {
+
+// Largest supported D/2 for the rotation tables (D <= 256).
+constexpr int kMaxPairs = 128;
+
+// Rotation frequencies as exact fixed-point phases: F[d] = theta_d / (2*pi)
+// in units of 2^-64 turns, reduced mod 1 turn.  The phase of an integer
+// offset p is then (uint64)(p * F[d]) mod 2^64 -- the multiply wraps for
+// free, negative p included -- so a rotation angle never loses the bits that
+// an fp32 product p*theta_d would drop at p ~ 1e5.
+struct PhaseTable {
+    unsigned long long f[kMaxPairs];
+};
+
+// Host: fill F[d] for d < D/2 (theta_d = theta^(-2d/D), the RoPE frequencies
+// of the "local RoPE-faithful window").  Returns false on bad arguments.
+bool make_phase_table(PhaseTable *t, int D, double theta);
+
+// Host: group factor g = max(1, ceil(s / L)) -- the smallest integer g with
+// floor((s-1)/g) <= L-1 (ResearchPod summary: smallest integer grouping).
+inline int64_t group_factor_host(int64_t s, int64_t L) { return s <= L ? 1 : (s + L - 1) / L; }
+
+// Host: pointer to the device status word of the current device (cached per
+// device).  Returns nullptr if CUDA is unusable.
+int *status_word_ptr();
+
+// Host: cudaError -> JL status, clearing the sticky-free error state.
+int cuda_status(cudaError_t e);
+
+// Host: true when p is 16-byte aligned.
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------- device side
+
+// sin/cos of the angle p * theta_d given its fixed-point frequency F.
+// The top 32 bits of the 64-bit phase are a signed fraction of a half turn
+// in [-1, 1); sincospif evaluates it.
+__device__ __forceinline__ void phase_sincos(long long p, unsigned long long F, float *s, float *c)
+{
+    unsigned long long ph = static_cast<unsigned long long>(p) * F;
+    int hi = static_cast<int>(ph >> 32);
+    float x = static_cast<float>(hi) * 4.656612873077392578125e-10f;  // 2^-31
+    sincospif(x, s, c);
+}
+
+// floor(p / g) for p >= 0, g >= 1.
+__device__ __forceinline__ int grouped_pos(int p, int g) { return p / g; }
+
+// delta_p = floor(p/g) - p  (<= 0): the correction offset of position p.
+__device__ __forceinline__ int delta_pos(int p, int g) { return p / g - p; }
+
+__device__ __forceinline__ void record_status(int *status, int code)
+{
+    if (status) atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ unsigned long long globaltimer_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Upper bound of any single wait inside a kernel; far above the longest
+// legitimate wait (a few microseconds), far below a watchdog.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+// Two fp32 -> packed bf16x2 (round to nearest even); `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+}  // namespace jl
