@@ -79,8 +79,11 @@ __device__ __forceinline__ uint32_t sw128(int n, int cc)
     return (uint32_t)(n * 128 + ((cc ^ (n & 7)) << 4));
 }
 
-// Rotate rows of a 128-row tile (SW128 boxes) from src to dst by delta_p,
-// p = p0 + row, for the pairs this thread owns.  Thread t of the 128-thread
+// Rotate rows of a 128-row bf16 tile (SW128 boxes) from src to dst by
+// delta_p, p = p0 + row, for the pairs this thread owns, writing fp16: the
+// corrected operands feed a kind::f16 MMA with fp16 A and B, whose 11-bit
+// significand keeps the rounding of the aliased view ~8x below bf16's (the
+// rotation preserves each pair's norm, so |x| < 46000 stays finite).  Thread t of the 128-thread
 // group owns chunk pair c = t % CPR (pairs d = 8c..8c+7) and rows
 // n0 + RPS*k.  Angles: exact fixed-point phase at the first row, then a
 // recurrence of unit complex steps (delta moves by one of two constants per
@@ -142,8 +145,8 @@ struct Corrector {
                 float x0 = jl::bf16lo(av[e]), x1 = jl::bf16hi(av[e]);
                 float y0 = jl::bf16lo(bv[e]), y1 = jl::bf16hi(bv[e]);
                 const float c0 = zc[2 * e], s0 = zs[2 * e], c1 = zc[2 * e + 1], s1 = zs[2 * e + 1];
-                ao[e] = jl::pack_bf16x2(x0 * c0 - y0 * s0, x1 * c1 - y1 * s1);
-                bo[e] = jl::pack_bf16x2(y0 * c0 + x0 * s0, y1 * c1 + x1 * s1);
+                ao[e] = jl::pack_f16x2(x0 * c0 - y0 * s0, x1 * c1 - y1 * s1);
+                bo[e] = jl::pack_f16x2(y0 * c0 + x0 * s0, y1 * c1 + x1 * s1);
             }
             asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst + off_lo), "r"(ao[0]),
                          "r"(ao[1]), "r"(ao[2]), "r"(ao[3])
@@ -265,13 +268,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, false, false);
+            constexpr uint32_t idSG = idesc_f16_f32(kBM, kBN, false, false);
             constexpr uint32_t idPV = idesc_bf16_f32(kBM, D, false, true);
-            auto issue_qk = [&](uint32_t dcol, uint32_t a_base, uint32_t b_base) {
+            auto issue_qk = [&](uint32_t dcol, uint32_t a_base, uint32_t b_base, uint32_t idesc) {
 #pragma unroll
                 for (int k = 0; k < D / 16; k++) {
                     const uint32_t off = (k >> 2) * C::REGION + (k & 3) * 32;
-                    mma_bf16_ss(tS + dcol, sdesc_sw128(a_base + off, 16, 1024),
-                                sdesc_sw128(b_base + off, 16, 1024), idS, k > 0 ? 1u : 0u);
+                    mma_f16_ss(tS + dcol, sdesc_sw128(a_base + off, 16, 1024),
+                                sdesc_sw128(b_base + off, 16, 1024), idesc, k > 0 ? 1u : 0u);
                 }
             };
             bool ok = wait_bar(bar(C::B_QFULL), 0, wc);
@@ -288,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int k = 0; k < kBN / 16; k++) {
                     const uint32_t aoff = (k >> 2) * C::REGION + (k & 3) * 32;
-                    mma_bf16_ss(tO, sdesc_sw128(sP + aoff, 16, 1024),
+                    mma_f16_ss(tO, sdesc_sw128(sP + aoff, 16, 1024),
                                 sdesc_sw128(vb + k * 2048, C::REGION, 1024), idPV,
                                 (t > 0 || k > 0) ? 1u : 0u);
                 }
@@ -307,10 +311,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(ok = wait_bar(bar(C::B_KGFULL + s), (cu_par >> s) & 1, wc))) break;
                     cu_par ^= 1u << s;
                     tc_fence_after();
-                    issue_qk(128u * b0, sQG, kb);
+                    issue_qk(128u * b0, sQG, kb, idSG);
                 } else {
                     tc_fence_after();
-                    issue_qk(128u * b0, sQ, kb);
+                    issue_qk(128u * b0, sQ, kb, idS);
                 }
                 mma_commit(bar(C::B_SFULL + b0));
                 ub_par ^= 1u << b0;
@@ -321,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(ok = wait_bar(bar(C::B_KGFULL + s), (cu_par >> s) & 1, wc))) break;
                     cu_par ^= 1u << s;
                     tc_fence_after();
-                    issue_qk(128u * b1, sQG, kb);
+                    issue_qk(128u * b1, sQG, kb, idSG);
                     mma_commit(bar(C::B_SFULL + b1));
                     ub_par ^= 1u << b1;
                     slot += 2;
