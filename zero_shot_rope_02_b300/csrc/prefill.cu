@@ -9,19 +9,28 @@
 // - remote(window) on log-sum-exp statistics equals.  The aliased view is an
 // on-the-fly correction rotation of the exact-RoPE q/k held in shared memory.
 //
-// One CTA owns a 128-row query tile of one head and walks its key tiles
-// 0..diagonal.  A per-tile classifier picks the view: exact tiles run Q.K^T,
-// remote tiles run Qg.Kg^T on the K tile corrected in place, band tiles (the
-// ones the window edge crosses) run both and select per element.
+// One CTA owns a 128-row query tile of NH heads that share a kv head (GQA
+// pair when Hq/Hkv is even), so every K/V tile it loads and every K tile it
+// corrects serves 2 x 128 query rows.  Its key tiles are visited as a
+// sequence of "virtual tiles": first the remote phase -- every key tile
+// wholly outside the window plus the remote part of the tiles the window
+// edge crosses -- on Q corrected in place, then the exact phase -- the exact
+// part of those edge tiles plus every tile inside the window -- on Q
+// reloaded.  An edge tile thus appears twice with complementary masks; the
+// online softmax does not care in which order keys arrive.
 //
-// Warp roles (320 threads):
-//   warp 0      TMA producer (Q once, K/V tiles through an NS-stage ring)
-//   warp 1      TMEM allocator + single-thread tcgen05.mma issuer
-//   warps 2-5   softmax (one query row per thread, TMEM lane = row) + epilogue
-//   warps 6-9   correction: Qg once, then every remote/band K tile in place
-// TMEM (512 columns): S0 [0,128), S1 [128,256), O [256, 256+D).
-// Shared memory: Q, Qg (SW128, two 64-column boxes when D = 128), NS K and V
-// stages, one P tile (bf16, SW128 K-major) -- all 1024-byte aligned.
+// Warp roles (448 threads):
+//   warps 0-3   softmax of head 0 (one query row per thread, TMEM lane = row)
+//   warps 4-7   softmax of head 1 (idle when NH = 1)
+//   warps 8-11  correction: Q of every head once, then every remote K tile
+//   warp 12     TMA producer: Q, K ring (NK stages), V ring (NV stages)
+//   warp 13     TMEM allocator + single-thread tcgen05.mma issuer
+// TMEM (512 columns): S_n at [128n, 128n+128) with P_n (bf16) written over
+// its first 64 columns, O_n at [256 + 128n, 256 + 128n + D).
+// MMA order per virtual tile v: PV_0(v), QK_0(v+1), PV_1(v), QK_1(v+1): the
+// QK of the next tile for a head follows that head's PV in the in-order
+// tensor pipe, so it may overwrite S_n/P_n without a wait, and each softmax
+// group works while the tensor core serves the other head.
 #include <math.h>
 #include <stdio.h>
 
@@ -34,34 +43,33 @@ namespace {
 using namespace jl::ptx;
 
 constexpr int kBM = 128, kBN = 128;
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;
 constexpr float kLn2 = 0.6931471805599453f;
 // Lazy rescaling: the running maximum used as the exponent offset is moved
 // only when a row's maximum grows by more than this (log2 units), so P stays
 // <= 2^8 and O is rarely rescaled in TMEM.
 constexpr float kRescaleThreshold = 8.0f;
 
-template <int D>
+template <int D, int NH>
 struct Cfg {
-    static constexpr int NS = (D == 128) ? 2 : 3;
-    static constexpr int REGION = kBM * 64 * 2;  // one 128-row x 64-column bf16 box: 16 KB
+    static constexpr int REGION = kBM * 64 * 2;  // one 128-row x 64-column box: 16 KB
     static constexpr int NREG = D / 64;          // boxes per 128-row tile
     static constexpr int TILE = kBM * D * 2;     // Q / K / V tile bytes
-    static constexpr int PBYTES = kBM * kBN * 2; // P tile bytes
+    static constexpr int NK = (D == 128) ? 3 : 4;                     // K ring stages
+    static constexpr int NV = (D == 128) ? (NH == 2 ? 2 : 3) : 4;     // V ring stages
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_QG = OFF_Q + TILE;
-    static constexpr int OFF_K = OFF_QG + TILE;
-    static constexpr int OFF_V = OFF_K + NS * TILE;
-    static constexpr int OFF_P = OFF_V + NS * TILE;
-    static constexpr int OFF_BAR = OFF_P + PBYTES;
-    static constexpr int BAR_BYTES = 256;
+    static constexpr int OFF_K = OFF_Q + NH * TILE;
+    static constexpr int OFF_V = OFF_K + NK * TILE;
+    static constexpr int OFF_BAR = OFF_V + NV * TILE;
+    static constexpr int BAR_BYTES = 512;
     static constexpr int SMEM = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
     // barrier indices
-    static constexpr int B_QFULL = 0, B_QGFULL = 1, B_KFULL = 2, B_VFULL = 2 + NS,
-                         B_KVEMPTY = 2 + 2 * NS, B_KGFULL = 2 + 3 * NS, B_SEDONE = 2 + 4 * NS,
-                         B_SFULL = 3 + 4 * NS, B_SEMPTY = 5 + 4 * NS, B_PFULL = 7 + 4 * NS,
-                         B_ODONE = 8 + 4 * NS, B_DRAIN = 9 + 4 * NS, NBAR = 10 + 4 * NS;
-    static_assert(NBAR * 8 <= 192, "barrier area");
+    static constexpr int B_QFULL = 0, B_QGFULL = 1, B_QFREE = 2, B_DRAIN = 3, B_KFULL = 4,
+                         B_KEMPTY = B_KFULL + NK, B_KGFULL = B_KEMPTY + NK, B_VFULL = B_KGFULL + NK,
+                         B_VEMPTY = B_VFULL + NV, B_SFULL = B_VEMPTY + NV, B_PFULL = B_SFULL + 2,
+                         B_ODONE = B_PFULL + 2, NBAR = B_ODONE + 2;
+    static constexpr int OFF_TMEM_SLOT = 448, OFF_ABORT = 452;
+    static_assert(NBAR * 8 <= OFF_TMEM_SLOT, "barrier area");
     static_assert(SMEM <= 232448, "shared memory budget");
 };
 
@@ -69,7 +77,7 @@ struct Params {
     __nv_bfloat16 *out;  // [B, S, Hq, D]
     float *lse;          // [B, Hq, S]
     int *status;
-    int B, Hq, Hkv, S, w, g, grp, n_qtiles;
+    int B, Hq, Hkv, S, w, g, grp, n_qtiles, pairs;  // pairs = grp / NH
     float scale_log2;    // tau * log2(e)
 };
 
@@ -79,49 +87,56 @@ __device__ __forceinline__ uint32_t sw128(int n, int cc)
     return (uint32_t)(n * 128 + ((cc ^ (n & 7)) << 4));
 }
 
-// Rotate rows of a 128-row bf16 tile (SW128 boxes) from src to dst by
-// delta_p, p = p0 + row, for the pairs this thread owns, writing fp16: the
-// corrected operands feed a kind::f16 MMA with fp16 A and B, whose 11-bit
-// significand keeps the rounding of the aliased view ~8x below bf16's (the
-// rotation preserves each pair's norm, so |x| < 46000 stays finite).  Thread t of the 128-thread
-// group owns chunk pair c = t % CPR (pairs d = 8c..8c+7) and rows
-// n0 + RPS*k.  Angles: exact fixed-point phase at the first row, then a
-// recurrence of unit complex steps (delta moves by one of two constants per
-// RPS rows).
+__device__ __forceinline__ float fast_exp2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Rotate rows of a 128-row bf16 tile (SW128 boxes) in place by delta_p,
+// p = p0 + row, for the pairs this thread owns, writing fp16: the corrected
+// operands feed a kind::f16 MMA with fp16 A and B, whose 11-bit significand
+// keeps the rounding of the aliased view ~8x below bf16's (the rotation
+// preserves each pair's norm, so |x| < 46000 stays finite).
+// Thread t of the 128-thread group owns chunk pair c = t % CPR (pairs
+// d = 8c..8c+7) and rows n0 + RPS*k.  Angles: exact fixed-point phase at the
+// first row, then a recurrence of unit complex steps (delta moves by one of
+// two constants per RPS rows).
 template <int D>
 struct Corrector {
     static constexpr int CPR = D / 16;       // chunk pairs per row
     static constexpr int RPS = 128 / CPR;    // rows per step
     static constexpr int STEPS = 128 / RPS;  // rows per thread
+    static constexpr uint32_t REGION = kBM * 64 * 2;
     int c, n0, g, rs;
     float ac[8], as_[8], bc[8], bs_[8];      // step rotations A, B
-    unsigned long long F[8];
+    const unsigned long long *F;             // this thread's 8 phases (parameter space)
 
     __device__ void init(int t, int g_, const jl::PhaseTable &pt)
     {
         c = t % CPR;
         n0 = t / CPR;
         g = g_;
+        F = pt.f + 8 * c;
         const int qs = RPS / g;
         rs = RPS % g;
 #pragma unroll
         for (int e = 0; e < 8; e++) {
-            F[e] = pt.f[8 * c + e];
             jl::phase_sincos(qs - RPS, F[e], &as_[e], &ac[e]);
             jl::phase_sincos(qs + 1 - RPS, F[e], &bs_[e], &bc[e]);
         }
     }
 
-    __device__ void run(uint32_t src, uint32_t dst, int p0) const
+    __device__ void run(uint32_t tile, int p0) const
     {
-        constexpr uint32_t REGION = Cfg<D>::REGION;
         float zc[8], zs[8];
-        int p = p0 + n0;
+        const int p = p0 + n0;
         const int dp = jl::delta_pos(p, g);
 #pragma unroll
         for (int e = 0; e < 8; e++) jl::phase_sincos(dp, F[e], &zs[e], &zc[e]);
         int jm = p % g;
-#pragma unroll
+#pragma unroll 1
         for (int k = 0; k < STEPS; k++) {
             const int n = n0 + RPS * k;
             uint32_t off_lo, off_hi;
@@ -135,10 +150,10 @@ struct Corrector {
             uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
             asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
                          : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
-                         : "r"(src + off_lo));
+                         : "r"(tile + off_lo));
             asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
                          : "=r"(b0), "=r"(b1), "=r"(b2), "=r"(b3)
-                         : "r"(src + off_hi));
+                         : "r"(tile + off_hi));
             uint32_t av[4] = {a0, a1, a2, a3}, bv[4] = {b0, b1, b2, b3}, ao[4], bo[4];
 #pragma unroll
             for (int e = 0; e < 4; e++) {
@@ -148,10 +163,10 @@ struct Corrector {
                 ao[e] = jl::pack_f16x2(x0 * c0 - y0 * s0, x1 * c1 - y1 * s1);
                 bo[e] = jl::pack_f16x2(y0 * c0 + x0 * s0, y1 * c1 + x1 * s1);
             }
-            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst + off_lo), "r"(ao[0]),
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(tile + off_lo), "r"(ao[0]),
                          "r"(ao[1]), "r"(ao[2]), "r"(ao[3])
                          : "memory");
-            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst + off_hi), "r"(bo[0]),
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(tile + off_hi), "r"(bo[0]),
                          "r"(bo[1]), "r"(bo[2]), "r"(bo[3])
                          : "memory");
             // advance the rotation by RPS rows
@@ -170,56 +185,95 @@ struct Corrector {
     }
 };
 
-template <int D>
+// The virtual-tile sequence of one query tile (identical in every role).
+// Key-tile classes are monotone in the key tile index kt: remote, then band
+// (the window edge), then exact.  The remote phase visits kt in [0, nr)
+// (remote and band tiles, remote part), the exact phase kt in [kb, qt]
+// (band and exact tiles, exact part).
+struct Visit {
+    int nr, kb, T;
+
+    __device__ void init(int i0, int qt, int S, int w, int g)
+    {
+        // first kt whose class is not remote; first kt whose class is exact
+        int lo = 0, hi = qt;  // class(qt) is never remote (distance 0 < w)
+        while (lo < hi) {
+            int mid = (lo + hi) >> 1;
+            if (jl::tile_class(i0, mid * kBN, kBM, kBN, S, w, g) == jl::kTileRemote) lo = mid + 1;
+            else hi = mid;
+        }
+        kb = lo;
+        lo = kb;
+        hi = qt + 1;
+        while (lo < hi) {
+            int mid = (lo + hi) >> 1;
+            if (jl::tile_class(i0, mid * kBN, kBM, kBN, S, w, g) == jl::kTileExact) hi = mid;
+            else lo = mid + 1;
+        }
+        nr = lo;  // tiles [0, nr) have a remote part
+        T = nr + (qt + 1 - kb);
+    }
+
+    __device__ __forceinline__ int kt(int v) const { return v < nr ? v : kb + (v - nr); }
+    __device__ __forceinline__ bool remote(int v) const { return v < nr; }
+};
+
+template <int D, int NH>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const Params p,
                    const __grid_constant__ jl::PhaseTable pt)
 {
-    using C = Cfg<D>;
-    constexpr int NS = C::NS;
+    using C = Cfg<D, NH>;
+    constexpr int NK = C::NK, NV = C::NV;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~(uintptr_t)1023);
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t sQ = sbase + C::OFF_Q, sQG = sbase + C::OFF_QG, sK = sbase + C::OFF_K,
-                   sV = sbase + C::OFF_V, sP = sbase + C::OFF_P;
+    const uint32_t sQ = sbase + C::OFF_Q, sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
     const uint32_t bar0 = sbase + C::OFF_BAR;
     auto bar = [&](int idx) -> uint32_t { return bar0 + 8u * (uint32_t)idx; };
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_BAR + 192);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_BAR + 196);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_BAR + C::OFF_TMEM_SLOT);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_BAR + C::OFF_ABORT);
     const WaitCtx wc{p.status, abort_flag};
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.x;
-    const int b = bh / p.Hq, h = bh % p.Hq, hk = h / p.grp;
+    int u = blockIdx.x;
+    const int hp = u % p.pairs;
+    u /= p.pairs;
+    const int hk = u % p.Hkv;
+    const int b = u / p.Hkv;
+    const int h0 = hk * p.grp + hp * NH;              // first head of this CTA
     const int qt = p.n_qtiles - 1 - (int)blockIdx.y;  // longest rows first
     const int i0 = qt * kBM;
-    const int T = qt + 1;                             // key tiles 0..qt
     const int S = p.S, w = p.w, g = p.g;
-    const bool any_corr = jl::tile_class(i0, 0, kBM, kBN, S, w, g) != jl::kTileExact;
+    Visit vis;
+    vis.init(i0, qt, S, w, g);
+    const int T = vis.T, NR = vis.nr;
 
     if (threadIdx.x == 0) {
         mbar_init(bar(C::B_QFULL), 1);
         mbar_init(bar(C::B_QGFULL), 128);
-        for (int s = 0; s < NS; s++) {
+        mbar_init(bar(C::B_QFREE), 1);
+        mbar_init(bar(C::B_DRAIN), 1);
+        for (int s = 0; s < NK; s++) {
             mbar_init(bar(C::B_KFULL + s), 1);
-            mbar_init(bar(C::B_VFULL + s), 1);
-            mbar_init(bar(C::B_KVEMPTY + s), 1);
+            mbar_init(bar(C::B_KEMPTY + s), 1);
             mbar_init(bar(C::B_KGFULL + s), 128);
         }
-        mbar_init(bar(C::B_SEDONE), 1);
-        mbar_init(bar(C::B_SFULL + 0), 1);
-        mbar_init(bar(C::B_SFULL + 1), 1);
-        mbar_init(bar(C::B_SEMPTY + 0), 128);
-        mbar_init(bar(C::B_SEMPTY + 1), 128);
-        mbar_init(bar(C::B_PFULL), 128);
-        mbar_init(bar(C::B_ODONE), 1);
-        mbar_init(bar(C::B_DRAIN), 1);
+        for (int s = 0; s < NV; s++) {
+            mbar_init(bar(C::B_VFULL + s), 1);
+            mbar_init(bar(C::B_VEMPTY + s), 1);
+        }
+        for (int n = 0; n < 2; n++) {
+            mbar_init(bar(C::B_SFULL + n), 1);
+            mbar_init(bar(C::B_PFULL + n), 128);
+            mbar_init(bar(C::B_ODONE + n), 1);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 1) {
+    if (warp == 13) {
         tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
     }
@@ -227,114 +281,115 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tS = tmem, tO = tmem + 256;
 
-    if (warp == 0) {
+    if (warp == 12) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             prefetch_tmap(&tq);
             prefetch_tmap(&tk);
             prefetch_tmap(&tv);
-            mbar_arrive_expect_tx(bar(C::B_QFULL), C::TILE);
+            auto load_q = [&]() {
+                mbar_arrive_expect_tx(bar(C::B_QFULL), NH * C::TILE);
 #pragma unroll
-            for (int r = 0; r < C::NREG; r++)
-                tma_load_4d(sQ + r * C::REGION, &tq, bar(C::B_QFULL), r * 64, h, i0, b);
+                for (int n = 0; n < NH; n++)
+#pragma unroll
+                    for (int r = 0; r < C::NREG; r++)
+                        tma_load_4d(sQ + n * C::TILE + r * C::REGION, &tq, bar(C::B_QFULL), r * 64,
+                                    h0 + n, i0, b);
+            };
+            load_q();
             int issued = 0;
-            for (int it = 0; it < T; it++) {
-                const int s = it % NS, u = it / NS;
-                if (!wait_bar(bar(C::B_KVEMPTY + s), (u & 1) ^ 1, wc)) break;
-                mbar_arrive_expect_tx(bar(C::B_KFULL + s), C::TILE);
-#pragma unroll
-                for (int r = 0; r < C::NREG; r++)
-                    tma_load_4d(sK + s * C::TILE + r * C::REGION, &tk, bar(C::B_KFULL + s), r * 64, hk,
-                                it * kBN, b);
-                mbar_arrive_expect_tx(bar(C::B_VFULL + s), C::TILE);
-#pragma unroll
-                for (int r = 0; r < C::NREG; r++)
-                    tma_load_4d(sV + s * C::TILE + r * C::REGION, &tv, bar(C::B_VFULL + s), r * 64, hk,
-                                it * kBN, b);
-                issued = it + 1;
-            }
-            if (*abort_flag) {
-                // let the copies already issued land before the CTA retires
-                drain_bar(bar(C::B_QFULL), 0);
-                for (int it = issued - NS < 0 ? 0 : issued - NS; it < issued; it++) {
-                    drain_bar(bar(C::B_KFULL + it % NS), (it / NS) & 1);
-                    drain_bar(bar(C::B_VFULL + it % NS), (it / NS) & 1);
+            bool ok = true;
+            for (int v = 0; v < T; v++) {
+                const int kt = vis.kt(v);
+                if (v == NR && NR > 0) {
+                    // the remote phase has finished reading the corrected Q
+                    if (!(ok = wait_bar(bar(C::B_QFREE), 0, wc))) break;
+                    load_q();
                 }
+                const int sk = v % NK, sv = v % NV;
+                if (!(ok = wait_bar(bar(C::B_KEMPTY + sk), ((v / NK) & 1) ^ 1, wc))) break;
+                mbar_arrive_expect_tx(bar(C::B_KFULL + sk), C::TILE);
+#pragma unroll
+                for (int r = 0; r < C::NREG; r++)
+                    tma_load_4d(sK + sk * C::TILE + r * C::REGION, &tk, bar(C::B_KFULL + sk), r * 64, hk,
+                                kt * kBN, b);
+                if (!(ok = wait_bar(bar(C::B_VEMPTY + sv), ((v / NV) & 1) ^ 1, wc))) break;
+                mbar_arrive_expect_tx(bar(C::B_VFULL + sv), C::TILE);
+#pragma unroll
+                for (int r = 0; r < C::NREG; r++)
+                    tma_load_4d(sV + sv * C::TILE + r * C::REGION, &tv, bar(C::B_VFULL + sv), r * 64, hk,
+                                kt * kBN, b);
+                issued = v + 1;
+            }
+            if (!ok) {
+                // let the copies already issued land before the CTA retires
+                for (int v = issued - NK < 0 ? 0 : issued - NK; v < issued; v++)
+                    drain_bar(bar(C::B_KFULL + v % NK), (v / NK) & 1);
+                for (int v = issued - NV < 0 ? 0 : issued - NV; v < issued; v++)
+                    drain_bar(bar(C::B_VFULL + v % NV), (v / NV) & 1);
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 13) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, false, false);
             constexpr uint32_t idSG = idesc_f16_f32(kBM, kBN, false, false);
             constexpr uint32_t idPV = idesc_bf16_f32(kBM, D, false, true);
-            auto issue_qk = [&](uint32_t dcol, uint32_t a_base, uint32_t b_base, uint32_t idesc) {
+            bool ok = wait_bar(bar(C::B_QFULL), 0, wc);
+            if (ok && NR > 0) ok = wait_bar(bar(C::B_QGFULL), 0, wc);
+            // waits before the QK of virtual tile v
+            auto prep_qk = [&](int v) -> bool {
+                const int sk = v % NK;
+                if (!wait_bar(bar(C::B_KFULL + sk), (v / NK) & 1, wc)) return false;
+                if (vis.remote(v)) {
+                    if (!wait_bar(bar(C::B_KGFULL + sk), (v / NK) & 1, wc)) return false;
+                } else if (v == NR && NR > 0) {
+                    if (!wait_bar(bar(C::B_QFULL), 1, wc)) return false;  // Q reloaded
+                }
+                tc_fence_after();
+                return true;
+            };
+            auto qk_head = [&](int v, int n) {
+                const uint32_t kb = sK + (v % NK) * C::TILE, qb = sQ + n * C::TILE;
+                const uint32_t id = vis.remote(v) ? idSG : idS;
 #pragma unroll
                 for (int k = 0; k < D / 16; k++) {
                     const uint32_t off = (k >> 2) * C::REGION + (k & 3) * 32;
-                    mma_f16_ss(tS + dcol, sdesc_sw128(a_base + off, 16, 1024),
-                                sdesc_sw128(b_base + off, 16, 1024), idesc, k > 0 ? 1u : 0u);
+                    mma_f16_ss(tmem + 128u * n, sdesc_sw128(qb + off, 16, 1024),
+                               sdesc_sw128(kb + off, 16, 1024), id, k > 0 ? 1u : 0u);
                 }
+                mma_commit(bar(C::B_SFULL + n));
             };
-            bool ok = wait_bar(bar(C::B_QFULL), 0, wc);
-            if (ok && any_corr) ok = wait_bar(bar(C::B_QGFULL), 0, wc);
-            uint32_t ub_par = 0;  // bit b: parity of the next fill of S buffer b
-            uint32_t cu_par = 0;  // bit s: parity of the next correction of stage s
-            int slot = 0;
-            auto issue_pv = [&](int t) -> bool {
-                const int s = t % NS;
-                if (!wait_bar(bar(C::B_PFULL), t & 1, wc)) return false;
-                if (!wait_bar(bar(C::B_VFULL + s), (t / NS) & 1, wc)) return false;
-                tc_fence_after();
-                const uint32_t vb = sV + s * C::TILE;
-#pragma unroll
-                for (int k = 0; k < kBN / 16; k++) {
-                    const uint32_t aoff = (k >> 2) * C::REGION + (k & 3) * 32;
-                    mma_f16_ss(tO, sdesc_sw128(sP + aoff, 16, 1024),
-                                sdesc_sw128(vb + k * 2048, C::REGION, 1024), idPV,
-                                (t > 0 || k > 0) ? 1u : 0u);
-                }
-                mma_commit(bar(C::B_KVEMPTY + s));
-                mma_commit(bar(C::B_ODONE));
-                return true;
+            auto finish_qk = [&](int v) {
+                mma_commit(bar(C::B_KEMPTY + v % NK));
+                if (v == NR - 1) mma_commit(bar(C::B_QFREE));
             };
-            for (int it = 0; ok && it < T; it++) {
-                const int cls = jl::tile_class(i0, it * kBN, kBM, kBN, S, w, g);
-                const int s = it % NS;
-                const uint32_t kb = sK + s * C::TILE;
-                if (!(ok = wait_bar(bar(C::B_KFULL + s), (it / NS) & 1, wc))) break;
-                const int b0 = slot & 1;
-                if (!(ok = wait_bar(bar(C::B_SEMPTY + b0), ((ub_par >> b0) & 1) ^ 1, wc))) break;
-                if (cls == jl::kTileRemote) {
-                    if (!(ok = wait_bar(bar(C::B_KGFULL + s), (cu_par >> s) & 1, wc))) break;
-                    cu_par ^= 1u << s;
-                    tc_fence_after();
-                    issue_qk(128u * b0, sQG, kb, idSG);
-                } else {
-                    tc_fence_after();
-                    issue_qk(128u * b0, sQ, kb, idS);
-                }
-                mma_commit(bar(C::B_SFULL + b0));
-                ub_par ^= 1u << b0;
-                if (cls == jl::kTileBand) {
-                    mma_commit(bar(C::B_SEDONE));
-                    const int b1 = b0 ^ 1;
-                    if (!(ok = wait_bar(bar(C::B_SEMPTY + b1), ((ub_par >> b1) & 1) ^ 1, wc))) break;
-                    if (!(ok = wait_bar(bar(C::B_KGFULL + s), (cu_par >> s) & 1, wc))) break;
-                    cu_par ^= 1u << s;
-                    tc_fence_after();
-                    issue_qk(128u * b1, sQG, kb, idSG);
-                    mma_commit(bar(C::B_SFULL + b1));
-                    ub_par ^= 1u << b1;
-                    slot += 2;
-                } else {
-                    slot += 1;
-                }
-                if (it >= 1 && !(ok = issue_pv(it - 1))) break;
+            if (ok && (ok = prep_qk(0))) {
+                for (int n = 0; n < NH; n++) qk_head(0, n);
+                finish_qk(0);
             }
-            if (ok) ok = issue_pv(T - 1);
+            for (int v = 0; ok && v < T; v++) {
+                const int sv = v % NV;
+                for (int n = 0; n < NH; n++) {
+                    if (!(ok = wait_bar(bar(C::B_PFULL + n), v & 1, wc))) break;
+                    if (n == 0 && !(ok = wait_bar(bar(C::B_VFULL + sv), (v / NV) & 1, wc))) break;
+                    tc_fence_after();
+                    const uint32_t vb = sV + sv * C::TILE;
+#pragma unroll
+                    for (int k = 0; k < kBN / 16; k++)
+                        mma_f16_ts(tmem + 256u + 128u * n, tmem + 128u * n + 8u * k,
+                                   sdesc_sw128(vb + k * 2048, C::REGION, 1024), idPV,
+                                   (v > 0 || k > 0) ? 1u : 0u);
+                    mma_commit(bar(C::B_ODONE + n));
+                    if (n == NH - 1) mma_commit(bar(C::B_VEMPTY + sv));
+                    if (v + 1 < T) {
+                        if (n == 0 && !(ok = prep_qk(v + 1))) break;
+                        qk_head(v + 1, n);
+                        if (n == NH - 1) finish_qk(v + 1);
+                    }
+                }
+            }
             if (!ok) {
                 // make sure no MMA is still running before TMEM is released
                 mma_commit(bar(C::B_DRAIN));
@@ -342,159 +397,154 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
-    } else if (warp < 6) {
+    } else if (warp < 8) {
         // ------------------------------------------------------------ softmax
-        const int q4 = warp & 3;
-        const int row = 32 * q4 + lane;
-        const int i = i0 + row;
-        const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
-        float m_used = -INFINITY, l = 0.f;
-        uint32_t ub_par = 0;  // bit b: parity of the next fill of S buffer b
-        int slot = 0;
-        bool ok = true;
-        // the score of column e of a 32-column chunk, scaled to log2 units and
-        // masked (causal, past-the-end keys); band tiles select the view
-        auto score = [&](uint32_t xe, uint32_t ye, int j, bool band, bool need_mask) -> float {
-            float sv = __uint_as_float(xe);
-            if (band && i - j >= w) sv = __uint_as_float(ye);
-            if ((band || need_mask) && (j > i || j >= S)) return -INFINITY;
-            return sv * p.scale_log2;
-        };
-        for (int it = 0; it < T; it++) {
-            const int cls = jl::tile_class(i0, it * kBN, kBM, kBN, S, w, g);
-            const int j0 = it * kBN;
-            const int b0 = slot & 1, b1 = b0 ^ 1;
-            const bool band = (cls == jl::kTileBand);
-            if (!(ok = wait_bar_warp(bar(C::B_SFULL + b0), (ub_par >> b0) & 1, wc))) break;
-            if (band && !(ok = wait_bar_warp(bar(C::B_SFULL + b1), (ub_par >> b1) & 1, wc))) break;
-            tc_fence_after();
-            const bool need_mask = (j0 + kBN - 1 > i0) || (j0 + kBN > S);
-            const uint32_t sx = tS + lane_base + 128u * b0, sy = tS + lane_base + 128u * b1;
-            // pass 1: row maximum
-            float mx = -INFINITY;
-#pragma unroll 1
-            for (int ch = 0; ch < kBN / 32; ch++) {
-                uint32_t x[32], y[32];
-                tmem_ld32(sx + 32u * ch, x);
-                if (band) tmem_ld32(sy + 32u * ch, y);
-                tmem_ld_wait();
-#pragma unroll
-                for (int e = 0; e < 32; e++)
-                    mx = fmaxf(mx, score(x[e], band ? y[e] : 0u, j0 + 32 * ch + e, band, need_mask));
-            }
-            const float m_new = fmaxf(m_used, mx);
-            const bool rescale = m_new > m_used + kRescaleThreshold;
-            float factor = 1.f;
-            if (rescale) {
-                factor = exp2f(m_used - m_new);
-                m_used = m_new;
-                l *= factor;
-            }
-            // P buffer and O are free once PV of the previous tile is done
-            if (it >= 1) {
-                if (!(ok = wait_bar_warp(bar(C::B_ODONE), (it - 1) & 1, wc))) break;
+        const int n = warp >> 2;  // head slot
+        if (n < NH) {
+            const int q4 = warp & 3;
+            const int row = 32 * q4 + lane;
+            const int i = i0 + row;
+            const int h = h0 + n;
+            const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+            const uint32_t tS = tmem + lane_base + 128u * n;
+            const uint32_t tO = tmem + lane_base + 256u + 128u * n;
+            const float sc = p.scale_log2;
+            float m_used = -INFINITY, l = 0.f;  // m_used in log2 units
+            bool ok = true;
+            for (int v = 0; v < T; v++) {
+                const int kt = vis.kt(v);
+                const bool remote = vis.remote(v);
+                const int j0 = kt * kBN;
+                const bool band = jl::tile_class(i0, j0, kBM, kBN, S, w, g) == jl::kTileBand;
+                const bool causal = (j0 + kBN - 1 > i0) || (j0 + kBN > S);
+                // key j of this virtual tile is dropped when it is in the future,
+                // past the end, or (edge tiles) belongs to the other view
+                auto dropped = [&](int j) -> bool {
+                    bool d = causal && (j > i || j >= S);
+                    if (band) d = d || (remote ? (i - j < w) : (i - j >= w));
+                    return d;
+                };
+                if (!(ok = wait_bar_warp(bar(C::B_SFULL + n), v & 1, wc))) break;
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, rescale)) {
+                // pass 1: row maximum of the raw scores
+                float mx = -INFINITY;
+#pragma unroll 1
+                for (int ch = 0; ch < kBN / 32; ch++) {
+                    uint32_t x[32];
+                    tmem_ld32(tS + 32u * ch, x);
+                    tmem_ld_wait();
+                    if (causal || band) {
 #pragma unroll
+                        for (int e = 0; e < 32; e++)
+                            if (!dropped(j0 + 32 * ch + e)) mx = fmaxf(mx, __uint_as_float(x[e]));
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; e++) mx = fmaxf(mx, __uint_as_float(x[e]));
+                    }
+                }
+                const float m_new = fmaxf(m_used, mx * sc);
+                const bool rescale = m_new > m_used + kRescaleThreshold;
+                float factor = 1.f;
+                if (rescale) {
+                    factor = fast_exp2(m_used - m_new);
+                    m_used = m_new;
+                    l *= factor;
+                }
+                const float m_off = (m_used == -INFINITY) ? 0.f : m_used;
+                if (v >= 1 && __any_sync(0xffffffffu, rescale)) {
+                    // O holds PV of tiles < v (complete: this head's QK(v)
+                    // followed its PV(v-1) in the in-order tensor pipe)
+                    if (!(ok = wait_bar_warp(bar(C::B_ODONE + n), (v - 1) & 1, wc))) break;
+                    tc_fence_after();
+#pragma unroll 1
                     for (int ch = 0; ch < D / 32; ch++) {
                         uint32_t o[32];
-                        tmem_ld32(tO + lane_base + 32u * ch, o);
+                        tmem_ld32(tO + 32u * ch, o);
                         tmem_ld_wait();
 #pragma unroll
                         for (int e = 0; e < 32; e++) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
-                        tmem_st32(tO + lane_base + 32u * ch, o);
+                        tmem_st32(tO + 32u * ch, o);
                     }
                     tmem_st_wait();
                 }
-            }
-            // pass 2: P = 2^(score - m_used), bf16, into the SW128 K-major P tile
+                // pass 2: P = 2^(s*sc - m_off) as bf16 pairs over the first 64
+                // columns of S (chunk ch -> columns 16ch..16ch+15)
 #pragma unroll 1
-            for (int ch = 0; ch < kBN / 32; ch++) {
-                uint32_t x[32], y[32];
-                tmem_ld32(sx + 32u * ch, x);
-                if (band) tmem_ld32(sy + 32u * ch, y);
-                tmem_ld_wait();
-                uint32_t pk[16];
+                for (int ch = 0; ch < kBN / 32; ch++) {
+                    uint32_t x[32];
+                    tmem_ld32(tS + 32u * ch, x);
+                    tmem_ld_wait();
+                    uint32_t pk[16];
+                    if (causal || band) {
 #pragma unroll
-                for (int e = 0; e < 16; e++) {
-                    const int j = j0 + 32 * ch + 2 * e;
-                    const float p0 = exp2f(score(x[2 * e], band ? y[2 * e] : 0u, j, band, need_mask) - m_used);
-                    const float p1 =
-                        exp2f(score(x[2 * e + 1], band ? y[2 * e + 1] : 0u, j + 1, band, need_mask) - m_used);
-                    l += p0 + p1;
-                    pk[e] = jl::pack_bf16x2(p0, p1);
-                }
-                const uint32_t region = sP + (ch >> 1) * C::REGION;
+                        for (int e = 0; e < 16; e++) {
+                            const int j = j0 + 32 * ch + 2 * e;
+                            float p0 = dropped(j) ? 0.f : fast_exp2(fmaf(__uint_as_float(x[2 * e]), sc, -m_off));
+                            float p1 = dropped(j + 1) ? 0.f
+                                                      : fast_exp2(fmaf(__uint_as_float(x[2 * e + 1]), sc, -m_off));
+                            l += p0 + p1;
+                            pk[e] = jl::pack_bf16x2(p0, p1);
+                        }
+                    } else {
 #pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    const int cc = (ch & 1) * 4 + q;
-                    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(region + sw128(row, cc)),
-                                 "r"(pk[4 * q]), "r"(pk[4 * q + 1]), "r"(pk[4 * q + 2]), "r"(pk[4 * q + 3])
-                                 : "memory");
+                        for (int e = 0; e < 16; e++) {
+                            const float p0 = fast_exp2(fmaf(__uint_as_float(x[2 * e]), sc, -m_off));
+                            const float p1 = fast_exp2(fmaf(__uint_as_float(x[2 * e + 1]), sc, -m_off));
+                            l += p0 + p1;
+                            pk[e] = jl::pack_bf16x2(p0, p1);
+                        }
+                    }
+                    tmem_st16(tS + 16u * ch, pk);
                 }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(bar(C::B_PFULL + n));
             }
-            // S buffers fully read; P visible to the tensor core; O rescaled
-            tc_fence_before();
-            mbar_arrive(bar(C::B_SEMPTY + b0));
-            if (band) mbar_arrive(bar(C::B_SEMPTY + b1));
-            ub_par ^= 1u << b0;
-            if (band) ub_par ^= 1u << b1;
-            slot += band ? 2 : 1;
-            fence_proxy_async_smem();
-            mbar_arrive(bar(C::B_PFULL));
-        }
-        // ------------------------------------------------------------ epilogue
-        if (ok) ok = wait_bar_warp(bar(C::B_ODONE), (T - 1) & 1, wc);
-        if (ok) {
-            tc_fence_after();
-            const float inv_l = 1.f / l;
-            __nv_bfloat16 *orow = p.out + (((size_t)b * S + i) * p.Hq + h) * D;
+            // ------------------------------------------------------------ epilogue
+            if (ok) ok = wait_bar_warp(bar(C::B_ODONE + n), (T - 1) & 1, wc);
+            if (ok) {
+                tc_fence_after();
+                const float inv_l = 1.f / l;
+                __nv_bfloat16 *orow = p.out + (((size_t)b * S + i) * p.Hq + h) * D;
+#pragma unroll 1
+                for (int ch = 0; ch < D / 32; ch++) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + 32u * ch, o);
+                    tmem_ld_wait();
+                    uint32_t pk[16];
 #pragma unroll
-            for (int ch = 0; ch < D / 32; ch++) {
-                uint32_t o[32];
-                tmem_ld32(tO + lane_base + 32u * ch, o);
-                tmem_ld_wait();
-                uint32_t pk[16];
+                    for (int e = 0; e < 16; e++)
+                        pk[e] = jl::pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l,
+                                                __uint_as_float(o[2 * e + 1]) * inv_l);
+                    if (i < S) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * ch);
 #pragma unroll
-                for (int e = 0; e < 16; e++)
-                    pk[e] = jl::pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l,
-                                            __uint_as_float(o[2 * e + 1]) * inv_l);
-                if (i < S) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * ch);
-#pragma unroll
-                    for (int q = 0; q < 4; q++)
-                        dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                        for (int q = 0; q < 4; q++)
+                            dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                    }
                 }
+                if (i < S) p.lse[((size_t)b * p.Hq + h) * S + i] = (m_used + log2f(l)) * kLn2;
             }
-            if (i < S) p.lse[((size_t)b * p.Hq + h) * S + i] = (m_used + log2f(l)) * kLn2;
         }
     } else {
         // ------------------------------------------------------------ correction
-        if (any_corr) {
-            const int t = threadIdx.x - 192;
+        if (NR > 0) {
+            const int t = threadIdx.x - 256;
             Corrector<D> cor;
             cor.init(t, g, pt);
             bool ok = wait_bar_warp(bar(C::B_QFULL), 0, wc);
             if (ok) {
-                cor.run(sQ, sQG, i0);
+#pragma unroll 1
+                for (int n = 0; n < NH; n++) cor.run(sQ + n * C::TILE, i0);
                 fence_proxy_async_smem();
                 mbar_arrive(bar(C::B_QGFULL));
             }
-            int nb = 0;
-            for (int it = 0; ok && it < T; it++) {
-                const int cls = jl::tile_class(i0, it * kBN, kBM, kBN, S, w, g);
-                if (cls == jl::kTileExact) continue;
-                const int s = it % NS;
-                if (!(ok = wait_bar_warp(bar(C::B_KFULL + s), (it / NS) & 1, wc))) break;
-                if (cls == jl::kTileBand) {
-                    if (!(ok = wait_bar_warp(bar(C::B_SEDONE), nb & 1, wc))) break;
-                    nb++;
-                    tc_fence_after();
-                }
-                const uint32_t kb = sK + s * C::TILE;
-                cor.run(kb, kb, it * kBN);
+            for (int v = 0; ok && v < NR; v++) {
+                const int sk = v % NK;
+                if (!(ok = wait_bar_warp(bar(C::B_KFULL + sk), (v / NK) & 1, wc))) break;
+                cor.run(sK + sk * C::TILE, v * kBN);
                 fence_proxy_async_smem();
-                mbar_arrive(bar(C::B_KGFULL + s));
+                mbar_arrive(bar(C::B_KGFULL + sk));
             }
         }
     }
@@ -502,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, 512);
+    if (warp == 13) tmem_dealloc(tmem, 512);
 }
 
 // ---------------------------------------------------------------- host side
@@ -544,15 +594,16 @@ bool make_bshd_map(CUtensorMap *m, const void *base, int B, int S, int H, int D)
     return r == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, int NH>
 int launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const Params &p,
            const jl::PhaseTable &pt, cudaStream_t st)
 {
-    auto kern = prefill_kernel<D>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM);
+    auto kern = prefill_kernel<D, NH>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, NH>::SMEM);
     if (e != cudaSuccess) return jl::cuda_status(e);
-    dim3 grid((unsigned)(p.B * p.Hq), (unsigned)p.n_qtiles, 1);
-    kern<<<grid, kThreads, Cfg<D>::SMEM, st>>>(tq, tk, tv, p, pt);
+    dim3 grid((unsigned)(p.B * p.Hkv * p.pairs), (unsigned)p.n_qtiles, 1);
+    kern<<<grid, kThreads, Cfg<D, NH>::SMEM, st>>>(tq, tk, tv, p, pt);
     return jl::cuda_status(cudaGetLastError());
 }
 
@@ -591,7 +642,12 @@ extern "C" int jl_bifocal_prefill(const void *q, const void *k, const void *v, v
     p.g = (int)jl::group_factor_host(S, L_pre);
     p.grp = Hq / Hkv;
     p.n_qtiles = (int)n_qtiles;
+    // two heads of a GQA group per CTA when the group size is even
+    const int nh = (p.grp % 2 == 0) ? 2 : 1;
+    p.pairs = p.grp / nh;
     p.scale_log2 = (float)(1.0 / sqrt((double)D) * 1.4426950408889634);
     cudaStream_t st = (cudaStream_t)stream;
-    return D == 128 ? launch<128>(tq, tk, tv, p, pt, st) : launch<64>(tq, tk, tv, p, pt, st);
+    if (D == 128)
+        return nh == 2 ? launch<128, 2>(tq, tk, tv, p, pt, st) : launch<128, 1>(tq, tk, tv, p, pt, st);
+    return nh == 2 ? launch<64, 2>(tq, tk, tv, p, pt, st) : launch<64, 1>(tq, tk, tv, p, pt, st);
 }
