@@ -35,6 +35,15 @@ bool make_phase_table(PhaseTable *t, int D, double theta)
     return true;
 }
 
+void rotation_host(const PhaseTable &t, int d, long long offset, float *c, float *s)
+{
+    const unsigned long long ph = (unsigned long long)offset * t.f[d];
+    const double turns = (double)(long long)ph * 5.42101086242752217003726400434970855712890625e-20;  // 2^-64
+    const double a = turns * 6.283185307179586476925286766559;
+    *c = (float)cos(a);
+    *s = (float)sin(a);
+}
+
 int *status_word_ptr()
 {
     static int *cache[64] = {nullptr};

@@ -28,6 +28,10 @@ struct PhaseTable {
 // of the "local RoPE-faithful window").  Returns false on bad arguments.
 bool make_phase_table(PhaseTable *t, int D, double theta);
 
+// Host: cos / sin of the angle offset * theta_d, from the same exact
+// fixed-point phase the device uses, evaluated in double precision.
+void rotation_host(const PhaseTable &t, int d, long long offset, float *c, float *s);
+
 // Host: group factor g = max(1, ceil(s / L)) -- the smallest integer g with
 // floor((s-1)/g) <= L-1 (ResearchPod summary: smallest integer grouping).
 inline int64_t group_factor_host(int64_t s, int64_t L) { return s <= L ? 1 : (s + L - 1) / L; }
@@ -92,6 +96,70 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
 {
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Packed fp32 pairs (f32x2 arithmetic of the sm_100 family): one 64-bit
+// register holds (lo, hi); one instruction does two fp32 operations.
+typedef unsigned long long f32x2;
+
+__device__ __forceinline__ f32x2 f2(float lo, float hi)
+{
+    f32x2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void f2_split(f32x2 v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c)
+{
+    f32x2 r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b)
+{
+    f32x2 r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b)
+{
+    f32x2 r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+// Both bf16 halves of a packed word, widened exactly to an fp32 pair.
+__device__ __forceinline__ f32x2 bf16x2_to_f2(uint32_t u) { return f2(bf16lo(u), bf16hi(u)); }
+
+// fp32 pair -> packed fp16x2 (round to nearest even), lo in the low half.
+__device__ __forceinline__ uint32_t f2_to_f16x2(f32x2 v)
+{
+    float lo, hi;
+    f2_split(v, lo, hi);
+    return pack_f16x2(lo, hi);
+}
+
+// fp32 pair -> packed bf16x2 (round to nearest even), lo in the low half.
+__device__ __forceinline__ uint32_t f2_to_bf16x2(f32x2 v)
+{
+    float lo, hi;
+    f2_split(v, lo, hi);
+    return pack_bf16x2(lo, hi);
+}
+
+// Three-input fp32 maximum.
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
 }
 
 }  // namespace jl

@@ -19,12 +19,15 @@
 // reloaded.  An edge tile thus appears twice with complementary masks; the
 // online softmax does not care in which order keys arrive.
 //
-// Warp roles (448 threads):
+// Warp roles (480 threads):
 //   warps 0-3   softmax of head 0 (one query row per thread, TMEM lane = row)
 //   warps 4-7   softmax of head 1 (idle when NH = 1)
 //   warps 8-11  correction: Q of every head once, then every remote K tile
-//   warp 12     TMA producer: Q, K ring (NK stages), V ring (NV stages)
+//   warp 12     TMA producer: Q and the K ring (NK stages)
 //   warp 13     TMEM allocator + single-thread tcgen05.mma issuer
+//   warp 14     TMA producer: the V ring (NV stages), so K loads -- which the
+//               correction must finish before their QK -- never queue
+//               behind a V slot
 // TMEM (512 columns): S_n at [128n, 128n+128) with P_n (bf16) written over
 // its first 64 columns, O_n at [256 + 128n, 256 + 128n + D).
 // MMA order per virtual tile v: PV_0(v), QK_0(v+1), PV_1(v), QK_1(v+1): the
@@ -33,6 +36,7 @@
 // group works while the tensor core serves the other head.
 #include <math.h>
 #include <stdio.h>
+#include <string.h>
 
 #include "jl_common.cuh"
 #include "sm100_ptx.cuh"
@@ -43,7 +47,7 @@ namespace {
 using namespace jl::ptx;
 
 constexpr int kBM = 128, kBN = 128;
-constexpr int kThreads = 448;
+constexpr int kThreads = 480;
 constexpr float kLn2 = 0.6931471805599453f;
 // Lazy rescaling: the running maximum used as the exponent offset is moved
 // only when a row's maximum grows by more than this (log2 units), so P stays
@@ -94,93 +98,222 @@ __device__ __forceinline__ float fast_exp2(float x)
     return y;
 }
 
-// Rotate rows of a 128-row bf16 tile (SW128 boxes) in place by delta_p,
-// p = p0 + row, for the pairs this thread owns, writing fp16: the corrected
-// operands feed a kind::f16 MMA with fp16 A and B, whose 11-bit significand
-// keeps the rounding of the aliased view ~8x below bf16's (the rotation
-// preserves each pair's norm, so |x| < 46000 stays finite).
-// Thread t of the 128-thread group owns chunk pair c = t % CPR (pairs
-// d = 8c..8c+7) and rows n0 + RPS*k.  Angles: exact fixed-point phase at the
-// first row, then a recurrence of unit complex steps (delta moves by one of
-// two constants per RPS rows).
+// Unit rotations per rotation pair d, computed on the host from the exact
+// fixed-point phase, as cosine, sine and negated sine arrays (pairs of
+// consecutive d load as one f32x2): a = rotation by (RPS/g - RPS) * theta_d
+// (RPS rows further, no group boundary crossed), b = by (RPS/g + 1 - RPS) *
+// theta_d (one boundary crossed), a2 = by twice a.
+struct RotConsts {
+    alignas(8) float ac[64];
+    alignas(8) float as[64];
+    alignas(8) float ans[64];
+    alignas(8) float bc[64];
+    alignas(8) float bs[64];
+    alignas(8) float bns[64];
+    alignas(8) float a2c[64];
+    alignas(8) float a2s[64];
+    alignas(8) float a2ns[64];
+    int uni;  // g divides RPS: every RPS-row step is a
+};
+
+// Rotates 128-row bf16 tiles (SW128 boxes) in place by delta_p, p = p0 + row,
+// writing fp16: the corrected operands feed a kind::f16 MMA with fp16 A and
+// B, whose 11-bit significand keeps the rounding of the aliased view ~8x
+// below bf16's (the rotation preserves each pair's norm, so |x| < 46000
+// stays finite).  Thread t of the 128-thread group owns chunk pair
+// c = t % CPR (pairs d = 8c..8c+7) and rows n0 + RPS*k; the arithmetic runs
+// on packed fp32 pairs (two consecutive d per instruction).
+//
+// Angles.  When g divides RPS, delta moves by the same amount every RPS rows,
+// so two chains of unit complex numbers (even and odd steps of this thread's
+// rows, each advanced by a2) cover a tile with independent work, and after a
+// tile they have advanced exactly to the first rows of the next tile: the
+// remote K tiles come in order 0, 1, 2, ..., so the chains carry over and
+// are re-anchored from the exact phase only every kReanchorTiles tiles.
+// Otherwise every tile is anchored exactly and each step picks a or b.
 template <int D>
 struct Corrector {
     static constexpr int CPR = D / 16;       // chunk pairs per row
     static constexpr int RPS = 128 / CPR;    // rows per step
     static constexpr int STEPS = 128 / RPS;  // rows per thread
+    static constexpr int kReanchorTiles = 32;
     static constexpr uint32_t REGION = kBM * 64 * 2;
-    int c, n0, g, rs;
-    float ac[8], as_[8], bc[8], bs_[8];      // step rotations A, B
-    const unsigned long long *F;             // this thread's 8 phases (parameter space)
+    int c, n0, g, next_kt;
+    bool uni;
+    const unsigned long long *F;  // this thread's 8 phases (parameter space)
+    const RotConsts *rc;
+    jl::f32x2 ec[4], es[4], oc[4], os[4];  // chains: rows n0 and n0 + RPS of tile next_kt
 
-    __device__ void init(int t, int g_, const jl::PhaseTable &pt)
+    __device__ void init(int t, int g_, const jl::PhaseTable &pt, const RotConsts &rc_)
     {
         c = t % CPR;
         n0 = t / CPR;
         g = g_;
         F = pt.f + 8 * c;
-        const int qs = RPS / g;
-        rs = RPS % g;
+        rc = &rc_;
+        uni = rc_.uni != 0;
+        next_kt = -1;
+    }
+
+    __device__ __forceinline__ void offsets(int n, uint32_t &lo, uint32_t &hi) const
+    {
+        lo = sw128(n, c);
+        hi = (D == 128) ? REGION + lo : sw128(n, c + 4);
+    }
+
+    __device__ __forceinline__ static jl::f32x2 ld2(const float *p)
+    {
+        return *reinterpret_cast<const jl::f32x2 *>(p);
+    }
+
+    // (x, y) -> (x c - y s, y c + x s) for 8 pairs, fp16 out
+    __device__ __forceinline__ static void rotate(const uint32_t (&a)[4], const uint32_t (&b)[4],
+                                                  const jl::f32x2 (&zc)[4], const jl::f32x2 (&zs)[4],
+                                                  uint32_t (&ao)[4], uint32_t (&bo)[4])
+    {
 #pragma unroll
-        for (int e = 0; e < 8; e++) {
-            jl::phase_sincos(qs - RPS, F[e], &as_[e], &ac[e]);
-            jl::phase_sincos(qs + 1 - RPS, F[e], &bs_[e], &bc[e]);
+        for (int q = 0; q < 4; q++) {
+            const jl::f32x2 x = jl::bf16x2_to_f2(a[q]), y = jl::bf16x2_to_f2(b[q]);
+            const jl::f32x2 ny = y ^ 0x8000000080000000ull;
+            ao[q] = jl::f2_to_f16x2(jl::fma2(x, zc[q], jl::mul2(ny, zs[q])));
+            bo[q] = jl::f2_to_f16x2(jl::fma2(y, zc[q], jl::mul2(x, zs[q])));
         }
     }
 
-    __device__ void run(uint32_t tile, int p0) const
+    // z <- z * (cos + i sin) for the 8 pairs, given cos / sin / -sin arrays
+    __device__ __forceinline__ static void cmul(jl::f32x2 (&zc)[4], jl::f32x2 (&zs)[4],
+                                                const jl::f32x2 (&rcs)[4], const jl::f32x2 (&rsn)[4],
+                                                const jl::f32x2 (&rns)[4])
     {
-        float zc[8], zs[8];
-        const int p = p0 + n0;
-        const int dp = jl::delta_pos(p, g);
 #pragma unroll
-        for (int e = 0; e < 8; e++) jl::phase_sincos(dp, F[e], &zs[e], &zc[e]);
+        for (int q = 0; q < 4; q++) {
+            const jl::f32x2 nc = jl::fma2(zc[q], rcs[q], jl::mul2(zs[q], rns[q]));
+            const jl::f32x2 ns = jl::fma2(zs[q], rcs[q], jl::mul2(zc[q], rsn[q]));
+            zc[q] = nc;
+            zs[q] = ns;
+        }
+    }
+
+    __device__ __forceinline__ static void ld4(uint32_t addr, uint32_t (&r)[4])
+    {
+        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                     : "r"(addr));
+    }
+
+    __device__ __forceinline__ static void st4(uint32_t addr, const uint32_t (&r)[4])
+    {
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(r[0]), "r"(r[1]),
+                     "r"(r[2]), "r"(r[3])
+                     : "memory");
+    }
+
+    __device__ void sincos8(int off, jl::f32x2 (&zc)[4], jl::f32x2 (&zs)[4]) const
+    {
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            float s0, c0, s1, c1;
+            jl::phase_sincos(off, F[2 * q], &s0, &c0);
+            jl::phase_sincos(off, F[2 * q + 1], &s1, &c1);
+            zc[q] = jl::f2(c0, c1);
+            zs[q] = jl::f2(s0, s1);
+        }
+    }
+
+    // exact anchors of both chains at rows p and p + RPS
+    __device__ void anchor(int p)
+    {
+        sincos8(jl::delta_pos(p, g), ec, es);
+        sincos8(jl::delta_pos(p + RPS, g), oc, os);
+    }
+
+    // g divides RPS: rows n0 + 2k*RPS on the even chain, n0 + (2k+1)*RPS on
+    // the odd one, both advanced by a2 after every pair of rows
+    __device__ void run_uni(uint32_t tile)
+    {
+        jl::f32x2 rcs[4], rsn[4], rns[4];
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            rcs[q] = ld2(rc->a2c + 8 * c + 2 * q);
+            rsn[q] = ld2(rc->a2s + 8 * c + 2 * q);
+            rns[q] = ld2(rc->a2ns + 8 * c + 2 * q);
+        }
+#pragma unroll 1
+        for (int k = 0; k < STEPS / 2; k++) {
+            const int ne = n0 + 2 * k * RPS, no = ne + RPS;
+            uint32_t le, he, lo_, ho;
+            offsets(ne, le, he);
+            offsets(no, lo_, ho);
+            uint32_t a0[4], b0[4], a1[4], b1[4], r0[4], q0[4], r1[4], q1[4];
+            ld4(tile + le, a0);
+            ld4(tile + he, b0);
+            ld4(tile + lo_, a1);
+            ld4(tile + ho, b1);
+            rotate(a0, b0, ec, es, r0, q0);
+            rotate(a1, b1, oc, os, r1, q1);
+            st4(tile + le, r0);
+            st4(tile + he, q0);
+            st4(tile + lo_, r1);
+            st4(tile + ho, q1);
+            cmul(ec, es, rcs, rsn, rns);
+            cmul(oc, os, rcs, rsn, rns);
+        }
+    }
+
+    // any g: exact anchor at row n0, then per RPS rows a or b
+    __device__ void run_generic(uint32_t tile, int p0) const
+    {
+        jl::f32x2 zc[4], zs[4];
+        const int p = p0 + n0;
+        sincos8(jl::delta_pos(p, g), zc, zs);
+        const int rs = RPS % g;
         int jm = p % g;
 #pragma unroll 1
         for (int k = 0; k < STEPS; k++) {
-            const int n = n0 + RPS * k;
-            uint32_t off_lo, off_hi;
-            if (D == 128) {
-                off_lo = sw128(n, c);
-                off_hi = REGION + off_lo;
-            } else {
-                off_lo = sw128(n, c);
-                off_hi = sw128(n, c + 4);
-            }
-            uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-            asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                         : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
-                         : "r"(tile + off_lo));
-            asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                         : "=r"(b0), "=r"(b1), "=r"(b2), "=r"(b3)
-                         : "r"(tile + off_hi));
-            uint32_t av[4] = {a0, a1, a2, a3}, bv[4] = {b0, b1, b2, b3}, ao[4], bo[4];
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-                float x0 = jl::bf16lo(av[e]), x1 = jl::bf16hi(av[e]);
-                float y0 = jl::bf16lo(bv[e]), y1 = jl::bf16hi(bv[e]);
-                const float c0 = zc[2 * e], s0 = zs[2 * e], c1 = zc[2 * e + 1], s1 = zs[2 * e + 1];
-                ao[e] = jl::pack_f16x2(x0 * c0 - y0 * s0, x1 * c1 - y1 * s1);
-                bo[e] = jl::pack_f16x2(y0 * c0 + x0 * s0, y1 * c1 + x1 * s1);
-            }
-            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(tile + off_lo), "r"(ao[0]),
-                         "r"(ao[1]), "r"(ao[2]), "r"(ao[3])
-                         : "memory");
-            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(tile + off_hi), "r"(bo[0]),
-                         "r"(bo[1]), "r"(bo[2]), "r"(bo[3])
-                         : "memory");
-            // advance the rotation by RPS rows
+            uint32_t lo_, hi_;
+            offsets(n0 + RPS * k, lo_, hi_);
+            uint32_t a[4], b[4], ao[4], bo[4];
+            ld4(tile + lo_, a);
+            ld4(tile + hi_, b);
+            rotate(a, b, zc, zs, ao, bo);
+            st4(tile + lo_, ao);
+            st4(tile + hi_, bo);
             jm += rs;
             const bool carry = jm >= g;
             if (carry) jm -= g;
+            jl::f32x2 rcs[4], rsn[4], rns[4];
 #pragma unroll
-            for (int e = 0; e < 8; e++) {
-                const float sc = carry ? bc[e] : ac[e], ss = carry ? bs_[e] : as_[e];
-                const float nc = zc[e] * sc - zs[e] * ss;
-                const float ns = zs[e] * sc + zc[e] * ss;
-                zc[e] = nc;
-                zs[e] = ns;
+            for (int q = 0; q < 4; q++) {
+                const int i = 8 * c + 2 * q;
+                rcs[q] = ld2(carry ? rc->bc + i : rc->ac + i);
+                rsn[q] = ld2(carry ? rc->bs + i : rc->as + i);
+                rns[q] = ld2(carry ? rc->bns + i : rc->ans + i);
             }
+            cmul(zc, zs, rcs, rsn, rns);
+        }
+    }
+
+    // the query tile at rows p0..p0+127 (leaves the K chains to be re-anchored)
+    __device__ void run_q(uint32_t tile, int p0)
+    {
+        if (uni) {
+            anchor(p0 + n0);
+            run_uni(tile);
+            next_kt = -1;
+        } else {
+            run_generic(tile, p0);
+        }
+    }
+
+    // remote K tile kt (tiles arrive in increasing order)
+    __device__ void run_k(uint32_t tile, int kt)
+    {
+        if (uni) {
+            if (kt != next_kt || kt % kReanchorTiles == 0) anchor(kt * kBN + n0);
+            run_uni(tile);
+            next_kt = kt + 1;
+        } else {
+            run_generic(tile, kt * kBN);
         }
     }
 };
@@ -222,7 +355,7 @@ template <int D, int NH>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const Params p,
-                   const __grid_constant__ jl::PhaseTable pt)
+                   const __grid_constant__ jl::PhaseTable pt, const __grid_constant__ RotConsts rc)
 {
     using C = Cfg<D, NH>;
     constexpr int NK = C::NK, NV = C::NV;
@@ -283,11 +416,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 12) {
-        // ------------------------------------------------------------ producer
+        // ------------------------------------------------------------ producer: Q and K
         if (lane == 0) {
             prefetch_tmap(&tq);
             prefetch_tmap(&tk);
-            prefetch_tmap(&tv);
             auto load_q = [&]() {
                 mbar_arrive_expect_tx(bar(C::B_QFULL), NH * C::TILE);
 #pragma unroll
@@ -301,31 +433,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             int issued = 0;
             bool ok = true;
             for (int v = 0; v < T; v++) {
-                const int kt = vis.kt(v);
                 if (v == NR && NR > 0) {
                     // the remote phase has finished reading the corrected Q
                     if (!(ok = wait_bar(bar(C::B_QFREE), 0, wc))) break;
                     load_q();
                 }
-                const int sk = v % NK, sv = v % NV;
+                const int sk = v % NK;
                 if (!(ok = wait_bar(bar(C::B_KEMPTY + sk), ((v / NK) & 1) ^ 1, wc))) break;
                 mbar_arrive_expect_tx(bar(C::B_KFULL + sk), C::TILE);
 #pragma unroll
                 for (int r = 0; r < C::NREG; r++)
                     tma_load_4d(sK + sk * C::TILE + r * C::REGION, &tk, bar(C::B_KFULL + sk), r * 64, hk,
-                                kt * kBN, b);
-                if (!(ok = wait_bar(bar(C::B_VEMPTY + sv), ((v / NV) & 1) ^ 1, wc))) break;
-                mbar_arrive_expect_tx(bar(C::B_VFULL + sv), C::TILE);
-#pragma unroll
-                for (int r = 0; r < C::NREG; r++)
-                    tma_load_4d(sV + sv * C::TILE + r * C::REGION, &tv, bar(C::B_VFULL + sv), r * 64, hk,
-                                kt * kBN, b);
+                                vis.kt(v) * kBN, b);
                 issued = v + 1;
             }
             if (!ok) {
                 // let the copies already issued land before the CTA retires
                 for (int v = issued - NK < 0 ? 0 : issued - NK; v < issued; v++)
                     drain_bar(bar(C::B_KFULL + v % NK), (v / NK) & 1);
+            }
+        }
+    } else if (warp == 14) {
+        // ------------------------------------------------------------ producer: V
+        if (lane == 0) {
+            prefetch_tmap(&tv);
+            int issued = 0;
+            bool ok = true;
+            for (int v = 0; v < T; v++) {
+                const int sv = v % NV;
+                if (!(ok = wait_bar(bar(C::B_VEMPTY + sv), ((v / NV) & 1) ^ 1, wc))) break;
+                mbar_arrive_expect_tx(bar(C::B_VFULL + sv), C::TILE);
+#pragma unroll
+                for (int r = 0; r < C::NREG; r++)
+                    tma_load_4d(sV + sv * C::TILE + r * C::REGION, &tv, bar(C::B_VFULL + sv), r * 64, hk,
+                                vis.kt(v) * kBN, b);
+                issued = v + 1;
+            }
+            if (!ok) {
                 for (int v = issued - NV < 0 ? 0 : issued - NV; v < issued; v++)
                     drain_bar(bar(C::B_VFULL + v % NV), (v / NV) & 1);
             }
@@ -411,49 +555,100 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float sc = p.scale_log2;
             float m_used = -INFINITY, l = 0.f;  // m_used in log2 units
             bool ok = true;
+            const jl::f32x2 sc2 = jl::f2(sc, sc);
             for (int v = 0; v < T; v++) {
                 const int kt = vis.kt(v);
                 const bool remote = vis.remote(v);
                 const int j0 = kt * kBN;
                 const bool band = jl::tile_class(i0, j0, kBM, kBN, S, w, g) == jl::kTileBand;
-                const bool causal = (j0 + kBN - 1 > i0) || (j0 + kBN > S);
-                // key j of this virtual tile is dropped when it is in the future,
-                // past the end, or (edge tiles) belongs to the other view
-                auto dropped = [&](int j) -> bool {
-                    bool d = causal && (j > i || j >= S);
-                    if (band) d = d || (remote ? (i - j < w) : (i - j >= w));
-                    return d;
+                const bool masked = band || (j0 + kBN - 1 > i0) || (j0 + kBN > S);
+                // load score chunk ch (32 columns) as raw fp32 bits; keys that are in
+                // the future, past the end, or (edge tiles) of the other view -> -inf
+                auto load_chunk = [&](int ch, uint32_t (&x)[32]) {
+                    tmem_ld32(tS + 32u * ch, x);
+                    tmem_ld_wait();
+                    if (masked) {
+#pragma unroll
+                        for (int e = 0; e < 32; e++) {
+                            const int j = j0 + 32 * ch + e;
+                            bool d = (j > i || j >= S);
+                            if (band) d = d || (remote ? (i - j < w) : (i - j >= w));
+                            if (d) x[e] = 0xff800000u;
+                        }
+                    }
+                };
+                // P = 2^(s*sc - m) for one chunk, bf16 pairs into S columns 16ch..16ch+15
+                auto exp_chunk = [&](int ch, const uint32_t (&x)[32], jl::f32x2 nm, jl::f32x2 &lsum) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; e++) {
+                        const jl::f32x2 t = jl::fma2(jl::f2(__uint_as_float(x[2 * e]), __uint_as_float(x[2 * e + 1])),
+                                                     sc2, nm);
+                        float t0, t1;
+                        jl::f2_split(t, t0, t1);
+                        const float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
+                        const jl::f32x2 pp = jl::f2(p0, p1);
+                        lsum = jl::add2(lsum, pp);
+                        pk[e] = jl::f2_to_bf16x2(pp);
+                    }
+                    tmem_st16(tS + 16u * ch, pk);
                 };
                 if (!(ok = wait_bar_warp(bar(C::B_SFULL + n), v & 1, wc))) break;
                 tc_fence_after();
-                // pass 1: row maximum of the raw scores
-                float mx = -INFINITY;
+                // One pass over the scores, chunk by chunk, against a running
+                // exponent offset m_cur (log2 units).  A chunk whose maximum
+                // exceeds m_cur by more than the threshold raises m_cur by an
+                // integer k (so the chunks already written are rescaled by the
+                // exact power of two 2^-k), or sets it when the row had no key
+                // yet.  S is never read again after a chunk's P is written.
+                float m_cur = m_used;
+                jl::f32x2 lsum = jl::f2(0.f, 0.f);
 #pragma unroll 1
                 for (int ch = 0; ch < kBN / 32; ch++) {
                     uint32_t x[32];
-                    tmem_ld32(tS + 32u * ch, x);
-                    tmem_ld_wait();
-                    if (causal || band) {
+                    load_chunk(ch, x);
+                    float cm = -INFINITY;
 #pragma unroll
-                        for (int e = 0; e < 32; e++)
-                            if (!dropped(j0 + 32 * ch + e)) mx = fmaxf(mx, __uint_as_float(x[e]));
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 32; e++) mx = fmaxf(mx, __uint_as_float(x[e]));
+                    for (int e = 0; e < 16; e++)
+                        cm = jl::fmax3(cm, __uint_as_float(x[2 * e]), __uint_as_float(x[2 * e + 1]));
+                    cm *= sc;
+                    const bool raise = cm > m_cur + kRescaleThreshold;
+                    float f = 1.f;
+                    if (raise) {
+                        if (m_cur == -INFINITY) {
+                            m_cur = cm;  // earlier chunks of this row hold only zeros
+                        } else {
+                            const float k = fminf(ceilf(cm - m_cur), 200.f);
+                            m_cur += k;
+                            f = ldexpf(1.f, -(int)k);  // exact power of two
+                        }
                     }
+                    if (ch > 0 && __any_sync(0xffffffffu, raise && f != 1.f)) {
+                        lsum = jl::mul2(lsum, jl::f2(f, f));
+                        tmem_st_wait();  // the P chunks written so far have landed
+                        for (int c2 = 0; c2 < ch; c2++) {
+                            uint32_t pk[16];
+                            tmem_ld16(tS + 16u * c2, pk);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int e = 0; e < 16; e++)
+                                pk[e] = jl::f2_to_bf16x2(jl::mul2(jl::bf16x2_to_f2(pk[e]), jl::f2(f, f)));
+                            tmem_st16(tS + 16u * c2, pk);
+                        }
+                    }
+                    const float m_off = (m_cur == -INFINITY) ? 0.f : m_cur;
+                    exp_chunk(ch, x, jl::f2(-m_off, -m_off), lsum);
                 }
-                const float m_new = fmaxf(m_used, mx * sc);
-                const bool rescale = m_new > m_used + kRescaleThreshold;
-                float factor = 1.f;
-                if (rescale) {
-                    factor = fast_exp2(m_used - m_new);
-                    m_used = m_new;
-                    l *= factor;
-                }
-                const float m_off = (m_used == -INFINITY) ? 0.f : m_used;
-                if (v >= 1 && __any_sync(0xffffffffu, rescale)) {
-                    // O holds PV of tiles < v (complete: this head's QK(v)
-                    // followed its PV(v-1) in the in-order tensor pipe)
+                // the tile moved the row's offset: bring O and l to the new one
+                const bool moved = m_cur != m_used;
+                const bool need_o = moved && m_used != -INFINITY;
+                const float factor = need_o ? exp2f(m_used - m_cur) : (moved ? 0.f : 1.f);
+                l *= factor;
+                if (v >= 1 && __any_sync(0xffffffffu, need_o)) {
+                    // O holds PV of tiles < v (complete: this head's QK(v) followed
+                    // its PV(v-1) in the in-order tensor pipe); rows whose offset
+                    // did not move (or that have no key yet) scale by 1
+                    const float fo = need_o ? factor : 1.f;
                     if (!(ok = wait_bar_warp(bar(C::B_ODONE + n), (v - 1) & 1, wc))) break;
                     tc_fence_after();
 #pragma unroll 1
@@ -462,40 +657,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_ld32(tO + 32u * ch, o);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int e = 0; e < 32; e++) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
+                        for (int e = 0; e < 32; e++) o[e] = __float_as_uint(__uint_as_float(o[e]) * fo);
                         tmem_st32(tO + 32u * ch, o);
                     }
-                    tmem_st_wait();
                 }
-                // pass 2: P = 2^(s*sc - m_off) as bf16 pairs over the first 64
-                // columns of S (chunk ch -> columns 16ch..16ch+15)
-#pragma unroll 1
-                for (int ch = 0; ch < kBN / 32; ch++) {
-                    uint32_t x[32];
-                    tmem_ld32(tS + 32u * ch, x);
-                    tmem_ld_wait();
-                    uint32_t pk[16];
-                    if (causal || band) {
-#pragma unroll
-                        for (int e = 0; e < 16; e++) {
-                            const int j = j0 + 32 * ch + 2 * e;
-                            float p0 = dropped(j) ? 0.f : fast_exp2(fmaf(__uint_as_float(x[2 * e]), sc, -m_off));
-                            float p1 = dropped(j + 1) ? 0.f
-                                                      : fast_exp2(fmaf(__uint_as_float(x[2 * e + 1]), sc, -m_off));
-                            l += p0 + p1;
-                            pk[e] = jl::pack_bf16x2(p0, p1);
-                        }
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 16; e++) {
-                            const float p0 = fast_exp2(fmaf(__uint_as_float(x[2 * e]), sc, -m_off));
-                            const float p1 = fast_exp2(fmaf(__uint_as_float(x[2 * e + 1]), sc, -m_off));
-                            l += p0 + p1;
-                            pk[e] = jl::pack_bf16x2(p0, p1);
-                        }
-                    }
-                    tmem_st16(tS + 16u * ch, pk);
-                }
+                m_used = m_cur;
+                float l0, l1;
+                jl::f2_split(lsum, l0, l1);
+                l += l0 + l1;
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(bar(C::B_PFULL + n));
@@ -531,18 +700,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (NR > 0) {
             const int t = threadIdx.x - 256;
             Corrector<D> cor;
-            cor.init(t, g, pt);
+            cor.init(t, g, pt, rc);
             bool ok = wait_bar_warp(bar(C::B_QFULL), 0, wc);
             if (ok) {
 #pragma unroll 1
-                for (int n = 0; n < NH; n++) cor.run(sQ + n * C::TILE, i0);
+                for (int n = 0; n < NH; n++) cor.run_q(sQ + n * C::TILE, i0);
                 fence_proxy_async_smem();
                 mbar_arrive(bar(C::B_QGFULL));
             }
             for (int v = 0; ok && v < NR; v++) {
                 const int sk = v % NK;
                 if (!(ok = wait_bar_warp(bar(C::B_KFULL + sk), (v / NK) & 1, wc))) break;
-                cor.run(sK + sk * C::TILE, v * kBN);
+                cor.run_k(sK + sk * C::TILE, v);
                 fence_proxy_async_smem();
                 mbar_arrive(bar(C::B_KGFULL + sk));
             }
@@ -596,14 +765,14 @@ bool make_bshd_map(CUtensorMap *m, const void *base, int B, int S, int H, int D)
 
 template <int D, int NH>
 int launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const Params &p,
-           const jl::PhaseTable &pt, cudaStream_t st)
+           const jl::PhaseTable &pt, const RotConsts &rc, cudaStream_t st)
 {
     auto kern = prefill_kernel<D, NH>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, NH>::SMEM);
     if (e != cudaSuccess) return jl::cuda_status(e);
     dim3 grid((unsigned)(p.B * p.Hkv * p.pairs), (unsigned)p.n_qtiles, 1);
-    kern<<<grid, kThreads, Cfg<D, NH>::SMEM, st>>>(tq, tk, tv, p, pt);
+    kern<<<grid, kThreads, Cfg<D, NH>::SMEM, st>>>(tq, tk, tv, p, pt, rc);
     return jl::cuda_status(cudaGetLastError());
 }
 
@@ -646,8 +815,22 @@ extern "C" int jl_bifocal_prefill(const void *q, const void *k, const void *v, v
     const int nh = (p.grp % 2 == 0) ? 2 : 1;
     p.pairs = p.grp / nh;
     p.scale_log2 = (float)(1.0 / sqrt((double)D) * 1.4426950408889634);
+    // step rotations of the correction (rows per step: 16 at D = 128, 32 at D = 64)
+    RotConsts rc;
+    memset(&rc, 0, sizeof(rc));
+    const int rps = 128 / (D / 16);
+    const long long qs = rps / p.g;
+    rc.uni = (rps % p.g == 0) ? 1 : 0;
+    for (int d = 0; d < D / 2; d++) {
+        jl::rotation_host(pt, d, qs - rps, &rc.ac[d], &rc.as[d]);
+        jl::rotation_host(pt, d, qs + 1 - rps, &rc.bc[d], &rc.bs[d]);
+        jl::rotation_host(pt, d, 2 * (qs - rps), &rc.a2c[d], &rc.a2s[d]);
+        rc.ans[d] = -rc.as[d];
+        rc.bns[d] = -rc.bs[d];
+        rc.a2ns[d] = -rc.a2s[d];
+    }
     cudaStream_t st = (cudaStream_t)stream;
     if (D == 128)
-        return nh == 2 ? launch<128, 2>(tq, tk, tv, p, pt, st) : launch<128, 1>(tq, tk, tv, p, pt, st);
-    return nh == 2 ? launch<64, 2>(tq, tk, tv, p, pt, st) : launch<64, 1>(tq, tk, tv, p, pt, st);
+        return nh == 2 ? launch<128, 2>(tq, tk, tv, p, pt, rc, st) : launch<128, 1>(tq, tk, tv, p, pt, rc, st);
+    return nh == 2 ? launch<64, 2>(tq, tk, tv, p, pt, rc, st) : launch<64, 1>(tq, tk, tv, p, pt, rc, st);
 }
