@@ -163,6 +163,40 @@ int jl_bifocal_decode(const void *q, const void *k_cache, const void *v_cache, v
                       int w, double theta, void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * Size of the fixed device scratch behind jl_bifocal_decode_noalloc: 8 MiB,
+ * enough for B * Hq * splits * (D + 2) * 4 bytes of split partials plus the
+ * arrival counters (for example B = 1, Hq = 32, D = 128 at any cache length).
+ */
+#define JL_DECODE_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * jl_bifocal_decode without a workspace argument.  The paper has no
+ * counterpart to this entry point; it exists for callers that cannot
+ * allocate device memory -- for instance code that runs inside another
+ * runtime's fixed, pre-planned memory pool, or a plug-in that has no access
+ * to an allocator -- and so cannot provide the scratch jl_bifocal_decode
+ * asks for.  It computes exactly what jl_bifocal_decode computes, with the
+ * same arguments (minus workspace / ws_bytes) and the same return codes.
+ *
+ * Scratch: a file-scope device array of JL_DECODE_NOALLOC_SCRATCH_BYTES that
+ * every GPU loading this library holds until the process exits.  Shapes
+ * whose split partials do not fit (jl_bifocal_decode_workspace_size() above
+ * that size) are rejected with JL_ERR_WORKSPACE before anything runs.  The
+ * call allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ * routine.  It clears the array's arrival counters (cudaMemsetAsync on
+ * `stream`) and then launches on `stream`.
+ *
+ * The first call made with a given device current looks up the array's
+ * device address on that device (cudaGetSymbolAddress) and caches it; make
+ * that first call before any stream capture.  Every call shares the one
+ * array, so two calls whose executions overlap on the GPU (different
+ * streams, no ordering between them) race on it and give undefined results.
+ */
+int jl_bifocal_decode_noalloc(const void *q, const void *k_cache, const void *v_cache, void *out,
+                              float *lse, int B, int Hq, int Hkv, int n, int n_cap, int D,
+                              int L_pre, int w, double theta, void *stream);
+
+/*
  * Debug: aliased positions floor(p/g) for p in [0, S), g = g(S, L_pre),
  * written as int32 to out_dev[0..S).  Computed on the device by the same
  * integer code the kernels use.

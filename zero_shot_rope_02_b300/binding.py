@@ -30,7 +30,7 @@ JL_ERR_GUARD = -8
 EXPORTS = (
     "jl_status_string", "jl_version", "jl_group_factor", "jl_rope_apply", "jl_bifocal_prefill",
     "jl_bifocal_decode_workspace_size", "jl_bifocal_decode", "jl_debug_grouped_positions",
-    "jl_debug_tile_classes", "jl_debug_status",
+    "jl_debug_tile_classes", "jl_debug_status", "jl_bifocal_decode_noalloc",
 )
 
 
@@ -55,6 +55,8 @@ def _load() -> ctypes.CDLL:
         "jl_bifocal_decode_workspace_size": (sz, [i32, i32, i32, i32, i32]),
         "jl_bifocal_decode": (i32, [p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, i32, dbl,
                                     p, sz, p]),
+        "jl_bifocal_decode_noalloc": (i32, [p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, i32,
+                                            dbl, p]),
         "jl_debug_grouped_positions": (i32, [i64, i64, p, p]),
         "jl_debug_tile_classes": (i32, [i32, i32, i32, p, p]),
         "jl_debug_status": (i32, [ctypes.POINTER(ctypes.c_int)]),
@@ -181,6 +183,32 @@ def jl_bifocal_decode(q, k_cache, v_cache, n: int, L_pre: int, w: int, theta: fl
                                  Hkv, int(n), n_cap, D, int(L_pre), int(w), float(theta),
                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
                                  _stream(stream)))
+    return out, lse
+
+
+def jl_bifocal_decode_noalloc(q, k_cache, v_cache, n: int, L_pre: int, w: int, theta: float,
+                              out=None, lse=None, stream=None):
+    """jl_bifocal_decode with the library's fixed device scratch instead of a
+    workspace (for callers that cannot allocate device memory).  Calls whose
+    executions overlap on the GPU share that scratch and race."""
+    import torch
+
+    for t, nm in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, nm)
+    B, Hq, D = q.shape
+    _, n_cap, Hkv, Dk = k_cache.shape
+    if Dk != D or v_cache.shape != k_cache.shape or k_cache.shape[0] != B:
+        raise ValueError("caches must be [B, n_cap, Hkv, D] matching q")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    _need(out, torch.bfloat16, "out")
+    _need(lse, torch.float32, "lse")
+    _check("jl_bifocal_decode_noalloc",
+           lib.jl_bifocal_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse), B,
+                                         Hq, Hkv, int(n), n_cap, D, int(L_pre), int(w), float(theta),
+                                         _stream(stream)))
     return out, lse
 
 

@@ -549,3 +549,69 @@ extern "C" int jl_bifocal_decode(const void *q, const void *k_cache, const void 
     default: return launch<64, 8>(a, B, pt, st);
     }
 }
+
+// ---------------------------------------------------------------- no-allocation entry point
+// Decode for callers that must not allocate device memory: the split-KV
+// scratch lives in a fixed file-scope device array instead of a caller
+// workspace.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = (size_t)JL_DECODE_NOALLOC_SCRATCH_BYTES;
+
+// The scratch itself.  Every GPU that loads this library holds it until the
+// process exits.  In host code this name is only a stand-in for the device
+// object, never a device address: the address comes from
+// cudaGetSymbolAddress, per device.
+static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
+
+// Device address of g_decode_scratch on the current device, looked up on the
+// first call made with that device current and cached afterwards.
+void *noalloc_scratch_address(int *status)
+{
+    static void *addr[64] = {nullptr};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        *status = JL_ERR_CUDA;
+        return nullptr;
+    }
+    if (!addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_decode_scratch);
+        if (e != cudaSuccess || p == nullptr) {
+            cudaGetLastError();
+            *status = JL_ERR_CUDA;
+            return nullptr;
+        }
+        addr[dev] = p;
+    }
+    return addr[dev];
+}
+
+}  // namespace
+
+extern "C" int jl_bifocal_decode_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                                         void *out, float *lse, int B, int Hq, int Hkv, int n,
+                                         int n_cap, int D, int L_pre, int w, double theta,
+                                         void *stream)
+{
+    if (!q || !k_cache || !v_cache || !out || !lse) return JL_ERR_ARG;
+    if (B < 1 || Hq < 1 || Hkv < 1 || n < 1 || n_cap < n || L_pre < 1 || w < 1 ||
+        !(theta > 0.0) || Hq % Hkv != 0)
+        return JL_ERR_ARG;
+    if (D != 64 && D != 128) return JL_ERR_UNSUPPORTED;
+    const Plan p = make_plan(B, Hkv, n);
+    size_t off_ml = 0, off_o = 0;
+    const size_t need = ws_layout(B, Hq, Hkv, D, p, &off_ml, &off_o);
+    if (need > kNoAllocScratchBytes) return JL_ERR_WORKSPACE;  // beyond the fixed scratch
+    int status = JL_OK;
+    void *scratch = noalloc_scratch_address(&status);
+    if (!scratch) return status;
+    // the arrival counters must start at zero; the array keeps whatever the
+    // previous call (of any size) left in it
+    cudaError_t e = cudaMemsetAsync(scratch, 0, off_ml, (cudaStream_t)stream);
+    if (e != cudaSuccess) return jl::cuda_status(e);
+    return jl_bifocal_decode(q, k_cache, v_cache, out, lse, B, Hq, Hkv, n, n_cap, D, L_pre, w, theta,
+                             scratch, kNoAllocScratchBytes, stream);
+}
