@@ -136,7 +136,9 @@ int jl_bifocal_prefill(const void *q, const void *k, const void *v, void *out, f
 
 /*
  * Workspace bytes jl_bifocal_decode needs for these sizes (split-KV partial
- * statistics and one arrival counter per (batch, kv head)).  0 on bad sizes.
+ * statistics and one arrival counter per (batch, kv head)).  The value does
+ * not grow with n: a workspace sized once serves every cache length for the
+ * same (B, Hq, Hkv, D).  0 on bad sizes.
  */
 size_t jl_bifocal_decode_workspace_size(int B, int Hq, int Hkv, int n, int D);
 

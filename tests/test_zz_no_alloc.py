@@ -62,7 +62,7 @@ def test_noalloc_rejects_shapes_beyond_its_scratch(jl, dev):
     """Split partials above the fixed scratch size are refused before any launch."""
     import torch
 
-    B, Hq, Hkv, n, D = 64, 64, 8, 131072, 128
+    B, Hq, Hkv, n, D = 64, 512, 64, 131072, 128  # 4096 (batch, kv head) units
     assert jl.jl_bifocal_decode_workspace_size(B, Hq, Hkv, n, D) > (8 << 20)
     q = torch.zeros((B, Hq, D), dtype=torch.bfloat16, device=dev)
     kv = torch.zeros((B, 16, Hkv, D), dtype=torch.bfloat16, device=dev)  # never read

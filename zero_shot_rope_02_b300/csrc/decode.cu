@@ -4,460 +4,461 @@
 // fall outside the local window are corrected by the rotation R_{delta_j} at
 // lookup time (ResearchPod transcript on caching; Jet-Long abstract: the
 // correction is applied on the fly).  The query at position n-1 is corrected
-// once by R_{delta_{n-1}}.  HBM-bound: every CTA streams one contiguous chunk
-// of one kv head's keys and values with 128-bit non-allocating loads, serving
-// all Hq/Hkv query heads that share the kv head, and produces partial
-// log-sum-exp statistics; the last CTA of each (batch, kv head) to finish
-// merges the partials.
+// once by R_{delta_{n-1}}.
 //
-// Rotation angles along a thread's key sequence come from a recurrence: a
-// thread steps KPS keys at a time, and delta changes by one of two constants
-// per step, so the rotation is advanced by one of two precomputed unit
-// complex numbers and re-anchored from the exact fixed-point phase every
-// kReanchor steps.
+// HBM-bound.  A CTA owns one contiguous chunk of one kv head's keys and
+// serves all Hq/Hkv query heads of that kv head.  A producer warp streams the
+// chunk's K and V rows in 64-key blocks through a 3-stage TMA ring; four
+// compute warps score a block (correcting its remote keys), fold it into a
+// running log-sum-exp per head, and accumulate P.V, all from shared memory
+// in packed f32x2 arithmetic.  The last CTA of each (batch, kv head) to
+// finish merges the per-chunk partial statistics.
+//
+// Rotation angles of remote keys come from a chain of unit complex numbers:
+// a thread's keys are KPS apart and, when g divides KPS, delta changes by
+// the same amount every KPS keys, so each key's rotation is the previous one
+// times a constant; the chain is re-anchored from the exact fixed-point
+// phase every kReanchorBlocks blocks.  Other g take the exact phase per key.
 #include <math.h>
+#include <string.h>
 
 #include "jl_common.cuh"
+#include "sm100_ptx.cuh"
 
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kUnroll = 4;
-constexpr int kReanchor = 32;
+using namespace jl::ptx;
+
+constexpr int kCompute = 128;           // compute threads (4 warps)
+constexpr int kThreads = kCompute + 32; // + one producer warp
+constexpr int kKB = 64;                 // keys per block
+constexpr int kNS = 3;                  // TMA ring stages
+constexpr int kReanchorBlocks = 32;
 constexpr float kLn2 = 0.6931471805599453f;
 
-__device__ __forceinline__ uint4 ldg_stream(const uint4 *p)
-{
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
+// Host-computed rotation per KPS keys for the chained angles, per pair d,
+// as cosine / sine / negated-sine arrays (consecutive d load as one f32x2).
+struct DecRot {
+    alignas(8) float c[64];
+    alignas(8) float s[64];
+    alignas(8) float ns[64];
+    int uni;  // g divides KPS
+};
 
 struct DecodeArgs {
     const __nv_bfloat16 *q;  // [B, Hq, D]
-    const __nv_bfloat16 *k;  // [B, n_cap, Hkv, D]
-    const __nv_bfloat16 *v;
     __nv_bfloat16 *out;      // [B, Hq, D]
     float *lse;              // [B, Hq]
     int *counters;           // [B * Hkv]
     float *part_ml;          // [B, Hq, splits, 2]
     float *part_o;           // [B, Hq, splits, D]
     int *status;
-    int Hq, Hkv, n, n_cap, w, g, splits, chunk;
+    int Hq, Hkv, n, w, g, splits, chunk;
     float scale_log2;        // tau * log2(e)
 };
 
-// Shared-memory carve-up (floats): q[GRP][D], qg[GRP][D], sc[GRP][chunk],
-// red[KPS3][GRP][D], plus small reduction scratch.
+// Named barrier over the compute warps only (the producer warp never joins).
+__device__ __forceinline__ void compute_sync()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(kCompute) : "memory");
+}
+
 template <int D, int GRP>
-struct Smem {
-    static constexpr int VC = D / 8;            // threads per V row (phase 3)
-    static constexpr int KPS3 = kThreads / VC;  // keys per step in phase 3
-    static size_t bytes(int chunk)
-    {
-        return sizeof(float) * (size_t)(2 * GRP * D + GRP * chunk + KPS3 * GRP * D + 4 * GRP * 4 +
-                                        2 * GRP + 2 * GRP * 256);
-    }
+struct DecCfg {
+    static constexpr int BLOCK_BYTES = kKB * D * 2;  // one K or V block
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = OFF_K + kNS * BLOCK_BYTES;
+    static constexpr int OFF_Q = OFF_V + kNS * BLOCK_BYTES;   // fp32 [GRP][D] exact q
+    static constexpr int OFF_QG = OFF_Q + GRP * D * 4;        // fp32 [GRP][D] corrected q
+    static constexpr int OFF_SC = OFF_QG + GRP * D * 4;       // fp32 [GRP][kKB] scores / p
+    static constexpr int OFF_ST = OFF_SC + GRP * kKB * 4;     // fp32 m[GRP], l[GRP], fac[GRP]
+    static constexpr int OFF_MW = OFF_ST + 3 * GRP * 4 + 16;  // merge weights [GRP][256]
+    static constexpr int OFF_BAR = (OFF_MW + GRP * 256 * 4 + 15) / 16 * 16;
+    static constexpr int SMEM = OFF_BAR + 2 * kNS * 8 + 16;
+    // end-of-chunk reduction buffer [KPS3][GRP][D] fp32 aliases the K/V ring
+    static constexpr int VC = D / 8, KPS3 = kCompute / VC;
+    static_assert(KPS3 * GRP * D * 4 <= 2 * kNS * BLOCK_BYTES, "reduction buffer");
 };
 
 template <int D, int GRP>
-__global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a,
-                                                          const __grid_constant__ jl::PhaseTable pt)
+__global__ void __launch_bounds__(kThreads, 2)
+    decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                  const DecodeArgs a, const __grid_constant__ jl::PhaseTable pt,
+                  const __grid_constant__ DecRot rot)
 {
+    using C = DecCfg<D, GRP>;
     constexpr int HALF = D / 2;
-    constexpr int CPK = D / 16;           // threads per key in phase 1 (8 pairs each)
-    constexpr int KPS = kThreads / CPK;   // keys per step in phase 1
-    constexpr int VC = Smem<D, GRP>::VC;
-    constexpr int KPS3 = Smem<D, GRP>::KPS3;
+    constexpr int CPK = D / 16;          // threads per key in scoring (8 pairs each)
+    constexpr int KPS = kCompute / CPK;  // keys per scoring step (16 or 32)
+    constexpr int ITEMS = kKB / KPS;     // scoring steps per block
+    constexpr int VC = C::VC;            // threads per V row (8 dims each)
+    constexpr int KPS3 = C::KPS3;        // keys per PV step
+    constexpr int VITEMS = kKB / KPS3;
 
-    extern __shared__ __align__(16) float smem[];
-    float *sq = smem;                       // exact q, fp32
-    float *sqg = sq + GRP * D;              // corrected q
-    float *sc = sqg + GRP * D;              // [GRP][chunk] scores (log2 units) then p
-    float *red = sc + GRP * a.chunk;        // [KPS3][GRP][D]
-    float *wred = red + KPS3 * GRP * D;     // [4 warps][GRP] x 4
-    float *stat = wred + 4 * GRP * 4;       // m[GRP], l[GRP]
-    float *mw = stat + 2 * GRP;             // merge weights [GRP][256]
-    __shared__ int s_last;
+    extern __shared__ __align__(128) uint8_t smem[];
+    float *sq = reinterpret_cast<float *>(smem + C::OFF_Q);
+    float *sqg = reinterpret_cast<float *>(smem + C::OFF_QG);
+    float *sc = reinterpret_cast<float *>(smem + C::OFF_SC);
+    float *st_m = reinterpret_cast<float *>(smem + C::OFF_ST);
+    float *st_l = st_m + GRP;
+    float *st_f = st_l + GRP;
+    float *mw = reinterpret_cast<float *>(smem + C::OFF_MW);
+    const uint32_t sbase = smem_u32(smem);
+    auto full = [&](int s) -> uint32_t { return sbase + C::OFF_BAR + 8u * s; };
+    auto empty = [&](int s) -> uint32_t { return sbase + C::OFF_BAR + 8u * (kNS + s); };
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_BAR + 2 * kNS * 8);
+    volatile int &s_last = *reinterpret_cast<volatile int *>(smem + C::OFF_BAR + 2 * kNS * 8 + 4);
+    const WaitCtx wc{a.status, abort_flag};
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
     const int n = a.n, g = a.g;
     const int j_begin = split * a.chunk;
     const int j_end = min(n, j_begin + a.chunk);
-    const int cnt = j_end - j_begin;
-    const int i = n - 1;                    // query position
-    const int j_split = max(0, n - a.w);    // keys below are remote
+    const int nblk = (j_end - j_begin + kKB - 1) / kKB;
+    const int j_split = (g > 1) ? max(0, n - a.w) : 0;  // keys below are remote
 
-    // ---- phase 0: the GRP query heads of this kv head, exact and corrected
-    const __nv_bfloat16 *qb = a.q + ((size_t)b * a.Hq + (size_t)hk * GRP) * D;
-    for (int e = tid; e < GRP * D; e += kThreads) sq[e] = __bfloat162float(qb[e]);
-    __syncthreads();
-    if (g > 1) {
-        const int di = jl::delta_pos(i, g);
-        for (int d = tid; d < HALF; d += kThreads) {
-            float s, c;
-            jl::phase_sincos(di, pt.f[d], &s, &c);
-#pragma unroll
-            for (int h = 0; h < GRP; h++) {
-                float x0 = sq[h * D + d], x1 = sq[h * D + d + HALF];
-                sqg[h * D + d] = x0 * c - x1 * s;
-                sqg[h * D + d + HALF] = x1 * c + x0 * s;
-            }
+    if (tid == 0) {
+        for (int s = 0; s < kNS; s++) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), kCompute / 32);
         }
+        *abort_flag = 0;
+        fence_mbar_init();
     }
     __syncthreads();
 
-    // ---- phase 1: scores
-    {
-        const int c = tid % CPK, r = tid / CPK;
-        const size_t row_stride = (size_t)a.Hkv * D / 8;  // uint4 per position
-        const uint4 *kb = reinterpret_cast<const uint4 *>(a.k) +
-                          ((size_t)b * a.n_cap * a.Hkv + hk) * (D / 8);
-        float qr[GRP][16];
-
-        auto load_q = [&](const float *src) {
-#pragma unroll
-            for (int h = 0; h < GRP; h++)
-#pragma unroll
-                for (int e = 0; e < 8; e++) {
-                    qr[h][e] = src[h * D + 8 * c + e];
-                    qr[h][8 + e] = src[h * D + HALF + 8 * c + e];
-                }
-        };
-        // dot of one key chunk pair with the GRP queries, reduced over the CPK
-        // threads of the key; thread c then writes head(s) c, c+CPK, ...
-        auto score_key = [&](const float kx[16], int jj, bool valid) {
-            float part[GRP];
-#pragma unroll
-            for (int h = 0; h < GRP; h++) {
-                float acc = 0.f;
-#pragma unroll
-                for (int e = 0; e < 16; e++) acc = fmaf(qr[h][e], kx[e], acc);
-                part[h] = acc;
+    if (warp == kCompute / 32) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            prefetch_tmap(&tk);
+            prefetch_tmap(&tv);
+            int issued = 0;
+            bool ok = true;
+            for (int blk = 0; blk < nblk; blk++) {
+                const int s = blk % kNS;
+                if (!(ok = wait_bar(empty(s), ((blk / kNS) & 1) ^ 1, wc))) break;
+                mbar_arrive_expect_tx(full(s), 2 * C::BLOCK_BYTES);
+                const int row = j_begin + blk * kKB;
+                tma_load_4d(sbase + C::OFF_K + s * C::BLOCK_BYTES, &tk, full(s), 0, hk, row, b);
+                tma_load_4d(sbase + C::OFF_V + s * C::BLOCK_BYTES, &tv, full(s), 0, hk, row, b);
+                issued = blk + 1;
             }
-#pragma unroll
-            for (int h = 0; h < GRP; h++)
-#pragma unroll
-                for (int o = 1; o < CPK; o <<= 1) part[h] += __shfl_xor_sync(0xffffffffu, part[h], o);
-            if (valid) {
-#pragma unroll
-                for (int h = 0; h < GRP; h++)
-                    if (h % CPK == c) sc[h * a.chunk + (jj - j_begin)] = part[h] * a.scale_log2;
-            }
-        };
-
-        // remote keys [j_begin, min(j_end, j_split)) when g > 1
-        const int rem_end = (g > 1) ? min(j_end, j_split) : j_begin;
-        if (rem_end > j_begin) {
-            load_q(sqg);
-            const int q0 = KPS / g, r0 = KPS % g;
-            float sac[8], sas[8], sbc[8], sbs[8], zc[8], zs[8];
-#pragma unroll
-            for (int e = 0; e < 8; e++) {
-                jl::phase_sincos(q0 - KPS, pt.f[8 * c + e], &sas[e], &sac[e]);
-                jl::phase_sincos(q0 + 1 - KPS, pt.f[8 * c + e], &sbs[e], &sbc[e]);
-            }
-            int j = j_begin + r;
-            int jm = j % g;
-            int since = kReanchor;  // forces an exact anchor on the first key
-            // iterate in warp-uniform trip counts so the shuffles stay converged
-            const int nsteps = (rem_end - j_begin + KPS - 1) / KPS;
-            for (int s0 = 0; s0 < nsteps; s0 += kUnroll) {
-                uint4 lo[kUnroll], hi[kUnroll];
-#pragma unroll
-                for (int u = 0; u < kUnroll; u++) {
-                    int jj = j + u * KPS;
-                    if (s0 + u < nsteps && jj < rem_end) {
-                        const uint4 *row = kb + (size_t)jj * row_stride;
-                        lo[u] = ldg_stream(row + c);
-                        hi[u] = ldg_stream(row + c + CPK);
-                    } else {
-                        lo[u] = make_uint4(0, 0, 0, 0);
-                        hi[u] = lo[u];
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < kUnroll; u++) {
-                    if (s0 + u >= nsteps) break;  // uniform across the warp
-                    int jj = j + u * KPS;
-                    if (since >= kReanchor) {
-                        int dj = jl::delta_pos(jj, g);
-#pragma unroll
-                        for (int e = 0; e < 8; e++) jl::phase_sincos(dj, pt.f[8 * c + e], &zs[e], &zc[e]);
-                        since = 0;
-                    }
-                    uint32_t lw[4] = {lo[u].x, lo[u].y, lo[u].z, lo[u].w};
-                    uint32_t hw[4] = {hi[u].x, hi[u].y, hi[u].z, hi[u].w};
-                    float kx[16];
-#pragma unroll
-                    for (int e = 0; e < 4; e++) {
-                        float a0 = jl::bf16lo(lw[e]), a1 = jl::bf16hi(lw[e]);
-                        float b0 = jl::bf16lo(hw[e]), b1 = jl::bf16hi(hw[e]);
-                        kx[2 * e] = a0 * zc[2 * e] - b0 * zs[2 * e];
-                        kx[2 * e + 1] = a1 * zc[2 * e + 1] - b1 * zs[2 * e + 1];
-                        kx[8 + 2 * e] = b0 * zc[2 * e] + a0 * zs[2 * e];
-                        kx[8 + 2 * e + 1] = b1 * zc[2 * e + 1] + a1 * zs[2 * e + 1];
-                    }
-                    score_key(kx, jj, jj < rem_end);
-                    // advance the rotation to key jj + KPS
-                    jm += r0;
-                    bool carry = jm >= g;
-                    if (carry) jm -= g;
-#pragma unroll
-                    for (int e = 0; e < 8; e++) {
-                        float sc_ = carry ? sbc[e] : sac[e], ss_ = carry ? sbs[e] : sas[e];
-                        float nc = zc[e] * sc_ - zs[e] * ss_;
-                        float ns = zs[e] * sc_ + zc[e] * ss_;
-                        zc[e] = nc;
-                        zs[e] = ns;
-                    }
-                    since++;
-                }
-                j += kUnroll * KPS;
-            }
+            if (!ok)
+                for (int blk = issued - kNS < 0 ? 0 : issued - kNS; blk < issued; blk++)
+                    drain_bar(full(blk % kNS), (blk / kNS) & 1);
         }
-
-        // exact keys [max(j_begin, rem_end), j_end)
-        const int ex_begin = max(j_begin, rem_end);
-        if (ex_begin < j_end) {
-            load_q(sq);
-            const int nsteps = (j_end - ex_begin + KPS - 1) / KPS;
-            int j = ex_begin + r;
-            for (int s0 = 0; s0 < nsteps; s0 += kUnroll) {
-                uint4 lo[kUnroll], hi[kUnroll];
-#pragma unroll
-                for (int u = 0; u < kUnroll; u++) {
-                    int jj = j + u * KPS;
-                    if (s0 + u < nsteps && jj < j_end) {
-                        const uint4 *row = kb + (size_t)jj * row_stride;
-                        lo[u] = ldg_stream(row + c);
-                        hi[u] = ldg_stream(row + c + CPK);
-                    } else {
-                        lo[u] = make_uint4(0, 0, 0, 0);
-                        hi[u] = lo[u];
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < kUnroll; u++) {
-                    if (s0 + u >= nsteps) break;
-                    int jj = j + u * KPS;
-                    uint32_t lw[4] = {lo[u].x, lo[u].y, lo[u].z, lo[u].w};
-                    uint32_t hw[4] = {hi[u].x, hi[u].y, hi[u].z, hi[u].w};
-                    float kx[16];
-#pragma unroll
-                    for (int e = 0; e < 4; e++) {
-                        kx[2 * e] = jl::bf16lo(lw[e]);
-                        kx[2 * e + 1] = jl::bf16hi(lw[e]);
-                        kx[8 + 2 * e] = jl::bf16lo(hw[e]);
-                        kx[8 + 2 * e + 1] = jl::bf16hi(hw[e]);
-                    }
-                    score_key(kx, jj, jj < j_end);
-                }
-                j += kUnroll * KPS;
-            }
-        }
-    }
-    __syncthreads();
-
-    // ---- phase 2: per-head max and exp over the chunk
-    for (int h = 0; h < GRP; h++) {
-        float *row = sc + h * a.chunk;
-        float m = -INFINITY;
-        for (int t = tid; t < cnt; t += kThreads) m = fmaxf(m, row[t]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if (lane == 0) wred[warp * GRP + h] = m;
-    }
-    __syncthreads();
-    if (tid < GRP) {
-        float m = wred[tid];
-        for (int w_ = 1; w_ < kThreads / 32; w_++) m = fmaxf(m, wred[w_ * GRP + tid]);
-        stat[tid] = m;
-    }
-    __syncthreads();
-    for (int h = 0; h < GRP; h++) {
-        float *row = sc + h * a.chunk;
-        const float m = stat[h];
-        float l = 0.f;
-        for (int t = tid; t < cnt; t += kThreads) {
-            float p = exp2f(row[t] - m);
-            row[t] = p;
-            l += p;
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-        if (lane == 0) wred[4 * GRP + warp * GRP + h] = l;
-    }
-    __syncthreads();
-    if (tid < GRP) {
-        float l = 0.f;
-        for (int w_ = 0; w_ < kThreads / 32; w_++) l += wred[4 * GRP + w_ * GRP + tid];
-        stat[GRP + tid] = l;
-    }
-
-    // ---- phase 3: P . V over the chunk
-    {
-        const int dc = tid % VC, r = tid / VC;
-        const size_t row_stride = (size_t)a.Hkv * D / 8;
-        const uint4 *vb = reinterpret_cast<const uint4 *>(a.v) +
-                          ((size_t)b * a.n_cap * a.Hkv + hk) * (D / 8);
-        float acc[GRP][8];
-#pragma unroll
-        for (int h = 0; h < GRP; h++)
-#pragma unroll
-            for (int e = 0; e < 8; e++) acc[h][e] = 0.f;
-        for (int j = j_begin + r; j < j_end; j += kUnroll * KPS3) {
-            uint4 vv[kUnroll];
-#pragma unroll
-            for (int u = 0; u < kUnroll; u++) {
-                int jj = j + u * KPS3;
-                vv[u] = (jj < j_end) ? ldg_stream(vb + (size_t)jj * row_stride + dc) : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int u = 0; u < kUnroll; u++) {
-                int jj = j + u * KPS3;
-                if (jj >= j_end) break;
-                uint32_t vw[4] = {vv[u].x, vv[u].y, vv[u].z, vv[u].w};
-                float vx[8];
-#pragma unroll
-                for (int e = 0; e < 4; e++) {
-                    vx[2 * e] = jl::bf16lo(vw[e]);
-                    vx[2 * e + 1] = jl::bf16hi(vw[e]);
-                }
-#pragma unroll
-                for (int h = 0; h < GRP; h++) {
-                    float p = sc[h * a.chunk + (jj - j_begin)];
-#pragma unroll
-                    for (int e = 0; e < 8; e++) acc[h][e] = fmaf(p, vx[e], acc[h][e]);
-                }
-            }
-        }
-#pragma unroll
-        for (int h = 0; h < GRP; h++)
-#pragma unroll
-            for (int e = 0; e < 8; e++) red[(r * GRP + h) * D + dc * 8 + e] = acc[h][e];
-    }
-    __syncthreads();
-
-    // reduce over the KPS3 key slots; o[h][d] unnormalised
-    const size_t hq0 = (size_t)b * a.Hq + (size_t)hk * GRP;
-    if (a.splits == 1) {
-        for (int t = tid; t < GRP * D; t += kThreads) {
-            int h = t / D, d = t % D;
-            float o = 0.f;
-#pragma unroll
-            for (int r = 0; r < KPS3; r++) o += red[(r * GRP + h) * D + d];
-            a.out[(hq0 + h) * D + d] = __float2bfloat16_rn(o / stat[GRP + h]);
-        }
-        if (tid < GRP) a.lse[hq0 + tid] = (stat[tid] + log2f(stat[GRP + tid])) * kLn2;
         return;
     }
-    for (int t = tid; t < GRP * D; t += kThreads) {
-        int h = t / D, d = t % D;
+
+    // ---------------------------------------------------------------- compute
+    // exact and corrected query of the GRP heads of this kv head, fp32
+    const __nv_bfloat16 *qb = a.q + ((size_t)b * a.Hq + (size_t)hk * GRP) * D;
+    for (int e = tid; e < GRP * D; e += kCompute) sq[e] = __bfloat162float(qb[e]);
+    if (tid < GRP) {
+        st_m[tid] = -INFINITY;
+        st_l[tid] = 0.f;
+    }
+    compute_sync();
+    if (g > 1) {
+        const int di = jl::delta_pos(n - 1, g);
+        for (int d = tid; d < HALF; d += kCompute) {
+            float sn, cs;
+            jl::phase_sincos(di, pt.f[d], &sn, &cs);
+#pragma unroll
+            for (int h = 0; h < GRP; h++) {
+                const float x0 = sq[h * D + d], x1 = sq[h * D + d + HALF];
+                sqg[h * D + d] = x0 * cs - x1 * sn;
+                sqg[h * D + d + HALF] = x1 * cs + x0 * sn;
+            }
+        }
+    }
+    compute_sync();
+
+    // scoring layout: thread (c, r) owns pairs 8c..8c+7 of keys r + KPS*i
+    const int c = tid % CPK, r = tid / CPK;
+    // PV layout: thread (dc, r3) owns dims 8dc..8dc+7 of keys r3 + KPS3*i
+    const int dc = tid % VC, r3 = tid / VC;
+    jl::f32x2 qr[GRP][8];  // this thread's 16 query values per head (pairs of consecutive dims)
+    int qmode = -1;        // which query qr holds: 0 exact, 1 corrected
+    auto load_q = [&](int mode) {
+        const float *src = mode ? sqg : sq;
+#pragma unroll
+        for (int h = 0; h < GRP; h++)
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                qr[h][e] = jl::f2(src[h * D + 8 * c + 2 * e], src[h * D + 8 * c + 2 * e + 1]);
+                qr[h][4 + e] = jl::f2(src[h * D + HALF + 8 * c + 2 * e], src[h * D + HALF + 8 * c + 2 * e + 1]);
+            }
+        qmode = mode;
+    };
+    // rotation chain of this thread's next remote key
+    jl::f32x2 zc[4], zs[4];
+    int chain_next = -1;  // key the chain currently refers to
+    const bool uni = rot.uni != 0;
+    auto anchor = [&](int j) {
+        const int dj = jl::delta_pos(j, g);
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            float s0, c0, s1, c1;
+            jl::phase_sincos(dj, pt.f[8 * c + 2 * q], &s0, &c0);
+            jl::phase_sincos(dj, pt.f[8 * c + 2 * q + 1], &s1, &c1);
+            zc[q] = jl::f2(c0, c1);
+            zs[q] = jl::f2(s0, s1);
+        }
+    };
+    // the chain's per-KPS-keys rotation for this thread's pairs, in registers
+    jl::f32x2 rcs[4], rsn[4], rns[4];
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+        rcs[q] = *reinterpret_cast<const jl::f32x2 *>(rot.c + 8 * c + 2 * q);
+        rsn[q] = *reinterpret_cast<const jl::f32x2 *>(rot.s + 8 * c + 2 * q);
+        rns[q] = *reinterpret_cast<const jl::f32x2 *>(rot.ns + 8 * c + 2 * q);
+    }
+    jl::f32x2 acc[GRP][4];
+#pragma unroll
+    for (int h = 0; h < GRP; h++)
+#pragma unroll
+        for (int e = 0; e < 4; e++) acc[h][e] = jl::f2(0.f, 0.f);
+
+    bool ok = true;
+    for (int blk = 0; blk < nblk; blk++) {
+        const int s = blk % kNS;
+        if (!(ok = wait_bar_warp(full(s), (blk / kNS) & 1, wc))) break;
+        const int j0 = j_begin + blk * kKB;
+        const uint8_t *kblk = smem + C::OFF_K + s * C::BLOCK_BYTES;
+        const uint8_t *vblk = smem + C::OFF_V + s * C::BLOCK_BYTES;
+        const bool any_remote = j0 < j_split;
+        const bool any_exact = j0 + kKB > j_split;
+
+        // ---- scores of this block (log2 units), one pass per view present
+        for (int mode = any_remote ? 1 : 0; mode >= (any_exact ? 0 : 1); mode--) {
+            if (qmode != mode) load_q(mode);
+#pragma unroll 1
+            for (int it = 0; it < ITEMS; it++) {
+                const int kk = r + KPS * it;
+                const int j = j0 + kk;
+                const uint4 lo4 = *reinterpret_cast<const uint4 *>(kblk + kk * (D * 2) + 16 * c);
+                const uint4 hi4 = *reinterpret_cast<const uint4 *>(kblk + kk * (D * 2) + D + 16 * c);
+                const uint32_t lw[4] = {lo4.x, lo4.y, lo4.z, lo4.w};
+                const uint32_t hw[4] = {hi4.x, hi4.y, hi4.z, hi4.w};
+                jl::f32x2 kx[8];
+                if (mode == 1) {
+                    // corrected key: (x, y) -> (x c - y s, y c + x s)
+                    if (!uni || chain_next != j || ((j - j_begin) / kKB) % kReanchorBlocks == 0 && it == 0)
+                        anchor(j);
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        const jl::f32x2 x = jl::bf16x2_to_f2(lw[q]), y = jl::bf16x2_to_f2(hw[q]);
+                        const jl::f32x2 ny = y ^ 0x8000000080000000ull;
+                        kx[q] = jl::fma2(x, zc[q], jl::mul2(ny, zs[q]));
+                        kx[4 + q] = jl::fma2(y, zc[q], jl::mul2(x, zs[q]));
+                    }
+                    if (uni) {
+                        // advance the chain to key j + KPS
+#pragma unroll
+                        for (int q = 0; q < 4; q++) {
+                            const jl::f32x2 nc = jl::fma2(zc[q], rcs[q], jl::mul2(zs[q], rns[q]));
+                            const jl::f32x2 ns = jl::fma2(zs[q], rcs[q], jl::mul2(zc[q], rsn[q]));
+                            zc[q] = nc;
+                            zs[q] = ns;
+                        }
+                        chain_next = j + KPS;
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        kx[q] = jl::bf16x2_to_f2(lw[q]);
+                        kx[4 + q] = jl::bf16x2_to_f2(hw[q]);
+                    }
+                }
+                float part[GRP];
+#pragma unroll
+                for (int h = 0; h < GRP; h++) {
+                    jl::f32x2 t = jl::mul2(qr[h][0], kx[0]);
+#pragma unroll
+                    for (int e = 1; e < 8; e++) t = jl::fma2(qr[h][e], kx[e], t);
+                    float t0, t1;
+                    jl::f2_split(t, t0, t1);
+                    part[h] = t0 + t1;
+                }
+#pragma unroll
+                for (int h = 0; h < GRP; h++)
+#pragma unroll
+                    for (int o = 1; o < CPK; o <<= 1) part[h] += __shfl_xor_sync(0xffffffffu, part[h], o);
+                const bool mine = (j < j_split) == (mode == 1);
+                const bool valid = j < j_end;
+#pragma unroll
+                for (int h = 0; h < GRP; h++)
+                    if (h % CPK == c && mine)
+                        sc[h * kKB + kk] = valid ? part[h] * a.scale_log2 : -INFINITY;
+            }
+        }
+        compute_sync();
+
+        // ---- running log-sum-exp per head: warp h folds the block in
+        for (int h = warp; h < GRP; h += kCompute / 32) {
+            const float s0 = sc[h * kKB + lane], s1 = sc[h * kKB + lane + 32];
+            float bm = fmaxf(s0, s1);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
+            const float m_old = st_m[h];
+            const float m_new = fmaxf(m_old, bm);
+            const float off = (m_new == -INFINITY) ? 0.f : m_new;
+            const float p0 = exp2f(s0 - off), p1 = exp2f(s1 - off);
+            sc[h * kKB + lane] = p0;
+            sc[h * kKB + lane + 32] = p1;
+            float sum = p0 + p1;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            if (lane == 0) {
+                const float fac = (m_old == -INFINITY) ? 0.f : exp2f(m_old - off);
+                st_l[h] = st_l[h] * fac + sum;
+                st_m[h] = m_new;
+                st_f[h] = fac;
+            }
+        }
+        compute_sync();
+
+        // ---- P . V
+#pragma unroll
+        for (int h = 0; h < GRP; h++) {
+            const jl::f32x2 f = jl::f2(st_f[h], st_f[h]);
+#pragma unroll
+            for (int e = 0; e < 4; e++) acc[h][e] = jl::mul2(acc[h][e], f);
+        }
+#pragma unroll 2
+        for (int it = 0; it < VITEMS; it++) {
+            const int kk = r3 + KPS3 * it;
+            const uint4 v4 = *reinterpret_cast<const uint4 *>(vblk + kk * (D * 2) + 16 * dc);
+            const jl::f32x2 vx[4] = {jl::bf16x2_to_f2(v4.x), jl::bf16x2_to_f2(v4.y), jl::bf16x2_to_f2(v4.z),
+                                     jl::bf16x2_to_f2(v4.w)};
+#pragma unroll
+            for (int h = 0; h < GRP; h++) {
+                const float pv = sc[h * kKB + kk];
+                const jl::f32x2 p2 = jl::f2(pv, pv);
+#pragma unroll
+                for (int e = 0; e < 4; e++) acc[h][e] = jl::fma2(p2, vx[e], acc[h][e]);
+            }
+        }
+        // this warp is done with stage s (scores of the next block overwrite
+        // sc only after the next compute_sync, which every warp reaches after
+        // its PV)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty(s));
+        compute_sync();
+    }
+    if (!ok) return;
+
+    // ---- reduce the KPS3 key slots; o[h][d] unnormalised (buffer aliases the ring)
+    float *red = reinterpret_cast<float *>(smem + C::OFF_K);
+#pragma unroll
+    for (int h = 0; h < GRP; h++)
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            float lo, hi;
+            jl::f2_split(acc[h][e], lo, hi);
+            red[(r3 * GRP + h) * D + dc * 8 + 2 * e] = lo;
+            red[(r3 * GRP + h) * D + dc * 8 + 2 * e + 1] = hi;
+        }
+    compute_sync();
+    const size_t hq0 = (size_t)b * a.Hq + (size_t)hk * GRP;
+    if (a.splits == 1) {
+        for (int t = tid; t < GRP * D; t += kCompute) {
+            const int h = t / D, d = t % D;
+            float o = 0.f;
+#pragma unroll
+            for (int q = 0; q < KPS3; q++) o += red[(q * GRP + h) * D + d];
+            a.out[(hq0 + h) * D + d] = __float2bfloat16_rn(o / st_l[h]);
+        }
+        if (tid < GRP) a.lse[hq0 + tid] = (st_m[tid] + log2f(st_l[tid])) * kLn2;
+        return;
+    }
+    for (int t = tid; t < GRP * D; t += kCompute) {
+        const int h = t / D, d = t % D;
         float o = 0.f;
 #pragma unroll
-        for (int r = 0; r < KPS3; r++) o += red[(r * GRP + h) * D + d];
+        for (int q = 0; q < KPS3; q++) o += red[(q * GRP + h) * D + d];
         a.part_o[((hq0 + h) * a.splits + split) * D + d] = o;
     }
     if (tid < GRP) {
-        a.part_ml[((hq0 + tid) * a.splits + split) * 2 + 0] = stat[tid];
-        a.part_ml[((hq0 + tid) * a.splits + split) * 2 + 1] = stat[GRP + tid];
+        a.part_ml[((hq0 + tid) * a.splits + split) * 2 + 0] = st_m[tid];
+        a.part_ml[((hq0 + tid) * a.splits + split) * 2 + 1] = st_l[tid];
     }
     __threadfence();
-    __syncthreads();
+    compute_sync();
     if (tid == 0) {
-        int ticket = atomicAdd(&a.counters[b * a.Hkv + hk], 1);
+        const int ticket = atomicAdd(&a.counters[b * a.Hkv + hk], 1);
         s_last = (ticket == a.splits - 1);
     }
-    __syncthreads();
+    compute_sync();
     if (!s_last) return;
     __threadfence();
 
     // ---- last CTA of this (b, kv head): merge the partial statistics
-    // weights w_s = 2^(m_s - M) / L with M = max m_s, L = sum l_s 2^(m_s - M)
-    for (int h = 0; h < GRP; h++) {
+    // weights w_s = 2^(m_s - M) with M = max m_s; L = sum l_s w_s
+    for (int h = warp; h < GRP; h += kCompute / 32) {
         const float *ml = a.part_ml + (hq0 + h) * a.splits * 2;
         float m = -INFINITY;
-        for (int s = tid; s < a.splits; s += kThreads) m = fmaxf(m, __ldcg(ml + 2 * s));
+        for (int q = lane; q < a.splits; q += 32) m = fmaxf(m, __ldcg(ml + 2 * q));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if (lane == 0) wred[warp * GRP + h] = m;
-    }
-    __syncthreads();
-    if (tid < GRP) {
-        float m = wred[tid];
-        for (int w_ = 1; w_ < kThreads / 32; w_++) m = fmaxf(m, wred[w_ * GRP + tid]);
-        stat[tid] = m;
-    }
-    __syncthreads();
-    for (int h = 0; h < GRP; h++) {
-        const float *ml = a.part_ml + (hq0 + h) * a.splits * 2;
-        const float M = stat[h];
-        float l = 0.f;
-        for (int s = tid; s < a.splits; s += kThreads) {
-            float wgt = exp2f(__ldcg(ml + 2 * s) - M);
-            mw[h * 256 + s] = wgt;
-            l += wgt * __ldcg(ml + 2 * s + 1);
+        const float off = (m == -INFINITY) ? 0.f : m;
+        float L = 0.f;
+        for (int q = lane; q < a.splits; q += 32) {
+            const float wgt = exp2f(__ldcg(ml + 2 * q) - off);
+            mw[h * 256 + q] = wgt;
+            L += wgt * __ldcg(ml + 2 * q + 1);
         }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-        if (lane == 0) wred[4 * GRP + warp * GRP + h] = l;
+        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        if (lane == 0) {
+            st_m[h] = m;
+            st_l[h] = L;
+        }
     }
-    __syncthreads();
-    if (tid < GRP) {
-        float l = 0.f;
-        for (int w_ = 0; w_ < kThreads / 32; w_++) l += wred[4 * GRP + w_ * GRP + tid];
-        stat[GRP + tid] = l;
-    }
-    __syncthreads();
-    for (int t = tid; t < GRP * D; t += kThreads) {
-        int h = t / D, d = t % D;
+    compute_sync();
+    for (int t = tid; t < GRP * D; t += kCompute) {
+        const int h = t / D, d = t % D;
         const float *po = a.part_o + (hq0 + h) * a.splits * D + d;
         float o0 = 0.f, o1 = 0.f;
-        int s = 0;
-        for (; s + 1 < a.splits; s += 2) {
-            o0 = fmaf(mw[h * 256 + s], __ldcg(po + (size_t)s * D), o0);
-            o1 = fmaf(mw[h * 256 + s + 1], __ldcg(po + (size_t)(s + 1) * D), o1);
+        int q = 0;
+        for (; q + 1 < a.splits; q += 2) {
+            o0 = fmaf(mw[h * 256 + q], __ldcg(po + (size_t)q * D), o0);
+            o1 = fmaf(mw[h * 256 + q + 1], __ldcg(po + (size_t)(q + 1) * D), o1);
         }
-        if (s < a.splits) o0 = fmaf(mw[h * 256 + s], __ldcg(po + (size_t)s * D), o0);
-        a.out[(hq0 + h) * D + d] = __float2bfloat16_rn((o0 + o1) / stat[GRP + h]);
+        if (q < a.splits) o0 = fmaf(mw[h * 256 + q], __ldcg(po + (size_t)q * D), o0);
+        a.out[(hq0 + h) * D + d] = __float2bfloat16_rn((o0 + o1) / st_l[h]);
     }
-    if (tid < GRP) a.lse[hq0 + tid] = (stat[tid] + log2f(stat[GRP + tid])) * kLn2;
+    if (tid < GRP) a.lse[hq0 + tid] = (st_m[tid] + log2f(st_l[tid])) * kLn2;
     if (tid == 0) a.counters[b * a.Hkv + hk] = 0;  // ready for the next call
 }
 
-// Split plan: enough CTAs to keep every SM streaming, chunks of 256..2048
-// keys (a multiple of 64), at most 256 splits per (batch, kv head).
+// Split plan: two CTAs per SM (shared memory and registers allow two), at
+// most 256 splits per (batch, kv head), chunks a multiple of the 64-key block.
+// splits_cap bounds splits for every n, and the workspace is sized by it, so
+// one workspace serves every cache length for the same (B, Hq, Hkv, D).
 struct Plan {
-    int splits, chunk;
+    int splits, chunk, splits_cap;
 };
 
 Plan make_plan(int B, int Hkv, int n)
 {
-    const long long target_ctas = 148 * 4;
+    const long long target_ctas = 148 * 2;
     long long per_head = (target_ctas + (long long)B * Hkv - 1) / ((long long)B * Hkv);
     if (per_head < 1) per_head = 1;
+    if (per_head > 256) per_head = 256;
     long long chunk = (n + per_head - 1) / per_head;
-    chunk = (chunk + 63) / 64 * 64;
-    if (chunk < 256) chunk = 256;
-    if (chunk > 2048) chunk = 2048;
-    long long splits = (n + chunk - 1) / chunk;
-    if (splits > 256) {
-        splits = 256;
-        chunk = ((n + splits - 1) / splits + 63) / 64 * 64;
-        splits = (n + chunk - 1) / chunk;
-    }
-    return Plan{(int)splits, (int)chunk};
+    chunk = (chunk + kKB - 1) / kKB * kKB;
+    long long splits = (n + chunk - 1) / chunk;  // <= per_head
+    return Plan{(int)splits, (int)chunk, (int)per_head};
 }
 
 size_t ws_layout(int B, int Hq, int Hkv, int D, const Plan &p, size_t *off_ml, size_t *off_o)
 {
     size_t cnt = ((size_t)B * Hkv * sizeof(int) + 255) / 256 * 256;
-    size_t ml = ((size_t)B * Hq * p.splits * 2 * sizeof(float) + 255) / 256 * 256;
-    size_t o = (size_t)B * Hq * p.splits * D * sizeof(float);
+    size_t ml = ((size_t)B * Hq * p.splits_cap * 2 * sizeof(float) + 255) / 256 * 256;
+    size_t o = (size_t)B * Hq * p.splits_cap * D * sizeof(float);
     if (off_ml) *off_ml = cnt;
     if (off_o) *off_o = cnt + ml;
     return cnt + ml + o;
@@ -468,15 +469,56 @@ bool shapes_ok(int B, int Hq, int Hkv, int n, int D)
     return B >= 1 && Hq >= 1 && Hkv >= 1 && n >= 1 && Hq % Hkv == 0 && (D == 64 || D == 128);
 }
 
-template <int D, int GRP>
-int launch(const DecodeArgs &a, int B, const jl::PhaseTable &pt, cudaStream_t st)
+// Per-call host work that depends only on (D, theta, g) is cached per thread.
+struct HostCache {
+    int D = 0, g = 0;
+    double theta = 0.0;
+    jl::PhaseTable pt;
+    DecRot rot;
+};
+
+bool host_tables(int D, double theta, int g, const jl::PhaseTable **pt, const DecRot **rot)
 {
-    size_t smem = Smem<D, GRP>::bytes(a.chunk);
+    thread_local HostCache hc;
+    if (hc.D != D || hc.theta != theta || hc.g != g) {
+        if (!jl::make_phase_table(&hc.pt, D, theta)) return false;
+        memset(&hc.rot, 0, sizeof(hc.rot));
+        const int kps = kCompute / (D / 16);
+        hc.rot.uni = (kps % g == 0) ? 1 : 0;
+        const long long step = kps / g - kps;  // delta moves by this per KPS keys when g | KPS
+        for (int d = 0; d < D / 2; d++) {
+            jl::rotation_host(hc.pt, d, step, &hc.rot.c[d], &hc.rot.s[d]);
+            hc.rot.ns[d] = -hc.rot.s[d];
+        }
+        hc.D = D;
+        hc.theta = theta;
+        hc.g = g;
+    }
+    *pt = &hc.pt;
+    *rot = &hc.rot;
+    return true;
+}
+
+template <int D, int GRP>
+int launch(const DecodeArgs &a, int B, int n_cap, const void *k_cache, const void *v_cache,
+           const jl::PhaseTable &pt, const DecRot &rot, cudaStream_t st)
+{
+    using C = DecCfg<D, GRP>;
     auto kern = decode_kernel<D, GRP>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return jl::cuda_status(e);
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return jl::cuda_status(cudaGetLastError());
+    if (!attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return jl::cuda_status(e);
+        attr_set[dev] = true;
+    }
+    CUtensorMap tk, tv;
+    if (!jl::make_bshd_map(&tk, k_cache, B, n_cap, a.Hkv, D, D, kKB, false) ||
+        !jl::make_bshd_map(&tv, v_cache, B, n_cap, a.Hkv, D, D, kKB, false))
+        return JL_ERR_CUDA;
     dim3 grid(a.splits, a.Hkv, B);
-    kern<<<grid, kThreads, smem, st>>>(a, pt);
+    kern<<<grid, kThreads, C::SMEM, st>>>(tk, tv, a, pt, rot);
     return jl::cuda_status(cudaGetLastError());
 }
 
@@ -510,13 +552,13 @@ extern "C" int jl_bifocal_decode(const void *q, const void *k_cache, const void 
     size_t need = ws_layout(B, Hq, Hkv, D, p, &off_ml, &off_o);
     if (!workspace || ws_bytes < need) return JL_ERR_WORKSPACE;
     if (!jl::aligned16(workspace)) return JL_ERR_ALIGN;
-    jl::PhaseTable pt;
-    if (!jl::make_phase_table(&pt, D, theta)) return JL_ERR_ARG;
+    const int g = (int)jl::group_factor_host(n, L_pre);
+    const jl::PhaseTable *pt = nullptr;
+    const DecRot *rot = nullptr;
+    if (!host_tables(D, theta, g, &pt, &rot)) return JL_ERR_ARG;
 
     DecodeArgs a;
     a.q = (const __nv_bfloat16 *)q;
-    a.k = (const __nv_bfloat16 *)k_cache;
-    a.v = (const __nv_bfloat16 *)v_cache;
     a.out = (__nv_bfloat16 *)out;
     a.lse = lse;
     char *ws = (char *)workspace;
@@ -527,26 +569,25 @@ extern "C" int jl_bifocal_decode(const void *q, const void *k_cache, const void 
     a.Hq = Hq;
     a.Hkv = Hkv;
     a.n = n;
-    a.n_cap = n_cap;
     a.w = w;
-    a.g = (int)jl::group_factor_host(n, L_pre);
+    a.g = g;
     a.splits = p.splits;
     a.chunk = p.chunk;
     a.scale_log2 = (float)(1.0 / sqrt((double)D) * 1.4426950408889634);
     cudaStream_t st = (cudaStream_t)stream;
     if (D == 128) {
         switch (grp) {
-        case 1: return launch<128, 1>(a, B, pt, st);
-        case 2: return launch<128, 2>(a, B, pt, st);
-        case 4: return launch<128, 4>(a, B, pt, st);
-        default: return launch<128, 8>(a, B, pt, st);
+        case 1: return launch<128, 1>(a, B, n_cap, k_cache, v_cache, *pt, *rot, st);
+        case 2: return launch<128, 2>(a, B, n_cap, k_cache, v_cache, *pt, *rot, st);
+        case 4: return launch<128, 4>(a, B, n_cap, k_cache, v_cache, *pt, *rot, st);
+        default: return launch<128, 8>(a, B, n_cap, k_cache, v_cache, *pt, *rot, st);
         }
     }
     switch (grp) {
-    case 1: return launch<64, 1>(a, B, pt, st);
-    case 2: return launch<64, 2>(a, B, pt, st);
-    case 4: return launch<64, 4>(a, B, pt, st);
-    default: return launch<64, 8>(a, B, pt, st);
+    case 1: return launch<64, 1>(a, B, n_cap, k_cache, v_cache, *pt, *rot, st);
+    case 2: return launch<64, 2>(a, B, n_cap, k_cache, v_cache, *pt, *rot, st);
+    case 4: return launch<64, 4>(a, B, n_cap, k_cache, v_cache, *pt, *rot, st);
+    default: return launch<64, 8>(a, B, n_cap, k_cache, v_cache, *pt, *rot, st);
     }
 }
 

@@ -3,6 +3,7 @@
 // aliasing integer rules, the device status word and bounded waits.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -27,6 +28,12 @@ struct PhaseTable {
 // Host: fill F[d] for d < D/2 (theta_d = theta^(-2d/D), the RoPE frequencies
 // of the "local RoPE-faithful window").  Returns false on bad arguments.
 bool make_phase_table(PhaseTable *t, int D, double theta);
+
+// Host: TMA tensor map over a bf16 [B, S, H, D] tensor viewed as the 4-D
+// tensor {D, H, S, B}; box {box_d, 1, box_rows, 1}; 128-byte swizzle or none;
+// zero fill outside the tensor.  False if the driver refuses it.
+bool make_bshd_map(CUtensorMap *m, const void *base, int B, int S, int H, int D, int box_d,
+                   int box_rows, bool swizzle128);
 
 // Host: cos / sin of the angle offset * theta_d, from the same exact
 // fixed-point phase the device uses, evaluated in double precision.

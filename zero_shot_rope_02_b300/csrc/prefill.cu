@@ -725,44 +725,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------- host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn()
-{
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                             &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess) {
-            cudaGetLastError();
-            return nullptr;
-        }
-        fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
-    return fn;
-}
-
-// [B, S, H, D] bf16 viewed as a 4-D tensor {D, H, S, B}; box {64, 1, 128, 1},
-// 128-byte swizzle, zero fill outside the tensor.
-bool make_bshd_map(CUtensorMap *m, const void *base, int B, int S, int H, int D)
-{
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
-    cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)S * H * D * 2};
-    cuuint32_t box[4] = {64, 1, 128, 1};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
-                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 template <int D, int NH>
 int launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const Params &p,
            const jl::PhaseTable &pt, const RotConsts &rc, cudaStream_t st)
@@ -796,8 +758,9 @@ extern "C" int jl_bifocal_prefill(const void *q, const void *k, const void *v, v
     jl::PhaseTable pt;
     if (!jl::make_phase_table(&pt, D, theta)) return JL_ERR_ARG;
     CUtensorMap tq, tk, tv;
-    if (!make_bshd_map(&tq, q, B, S, Hq, D) || !make_bshd_map(&tk, k, B, S, Hkv, D) ||
-        !make_bshd_map(&tv, v, B, S, Hkv, D))
+    if (!jl::make_bshd_map(&tq, q, B, S, Hq, D, 64, 128, true) ||
+        !jl::make_bshd_map(&tk, k, B, S, Hkv, D, 64, 128, true) ||
+        !jl::make_bshd_map(&tv, v, B, S, Hkv, D, 64, 128, true))
         return JL_ERR_CUDA;
     Params p;
     p.out = (__nv_bfloat16 *)out;
