@@ -231,8 +231,11 @@ def time_calls(fn, stream, dev, reps):
 
 def decode_sweep(jl, dev, stream, peaks):
     """us per decode call at n = 8K/32K/128K, Hq=32, Hkv=8, D=128, L=32768,
-    w=4096; the caches are rotated over copies totalling > 2x L2 so every
-    call reads K/V from HBM."""
+    w=4096 (g = 1, 1, 4).  The caches are rotated over copies totalling more
+    than 2x L2 so every call reads K/V from HBM.  The calls are captured in a
+    CUDA graph and the graph is replayed, so the number is device time per
+    call, as in a serving loop; the eager per-call time (host enqueue
+    included) rides along."""
     import torch
 
     from zero_shot_rope_02_b300 import inputs
@@ -252,20 +255,28 @@ def decode_sweep(jl, dev, stream, peaks):
         lse = torch.empty((1, 32), dtype=torch.float32, device=dev)
         it = [0]
 
-        def call():
+        def call(st=None):
             c = it[0] % copies
             it[0] += 1
-            jl.jl_bifocal_decode(q, ks[c], vs[c], n, 32768, 4096, 1e6, workspace=ws, out=o, lse=lse,
-                                 stream=stream)
+            jl.jl_bifocal_decode(q, ks[c], vs[c], n, 32768, 4096, 1e6, workspace=ws, out=o, lse=lse, stream=st)
 
         for _ in range(5):
-            call()
-        reps = 200 if n < 100000 else 50
-        us = 1e3 * time_calls(call, stream, dev, reps)
+            call(stream)
+        eager_us = 1e3 * time_calls(lambda: call(stream), stream, dev, 50)
+        per_graph = copies * max(1, 64 // copies)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(per_graph):
+                call()  # the capture stream is current
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        reps = 10 if n < 100000 else 4
+        us = 1e3 * time_calls(graph.replay, stream, dev, reps) / per_graph
         gbs = nbytes / (us * 1e-6) / 1e9
         out[str(n)] = {"us_per_token": round(us, 2), "gbs": round(gbs, 1),
-                       "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4), "g": jl.jl_group_factor(n, 32768)}
-        del ks, vs
+                       "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4), "g": jl.jl_group_factor(n, 32768),
+                       "eager_us_per_call": round(eager_us, 2), "timing": "cuda graph replay"}
+        del ks, vs, graph
     return out
 
 

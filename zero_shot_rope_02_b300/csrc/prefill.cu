@@ -562,71 +562,77 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int j0 = kt * kBN;
                 const bool band = jl::tile_class(i0, j0, kBM, kBN, S, w, g) == jl::kTileBand;
                 const bool masked = band || (j0 + kBN - 1 > i0) || (j0 + kBN > S);
-                // load score chunk ch (32 columns) as raw fp32 bits; keys that are in
-                // the future, past the end, or (edge tiles) of the other view -> -inf
-                auto load_chunk = [&](int ch, uint32_t (&x)[32]) {
-                    tmem_ld32(tS + 32u * ch, x);
+                // load 64 score columns (half hh) as raw fp32 bits with both TMEM
+                // loads in flight; keys that are in the future, past the end, or
+                // (edge tiles) of the other view -> -inf
+                auto load_half = [&](int hh, uint32_t (&x)[64]) {
+                    tmem_ld32(tS + 64u * hh, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+                    tmem_ld32(tS + 64u * hh + 32u, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
                     tmem_ld_wait();
                     if (masked) {
 #pragma unroll
-                        for (int e = 0; e < 32; e++) {
-                            const int j = j0 + 32 * ch + e;
+                        for (int e = 0; e < 64; e++) {
+                            const int j = j0 + 64 * hh + e;
                             bool d = (j > i || j >= S);
                             if (band) d = d || (remote ? (i - j < w) : (i - j >= w));
                             if (d) x[e] = 0xff800000u;
                         }
                     }
                 };
-                // P = 2^(s*sc - m) for one chunk, bf16 pairs into S columns 16ch..16ch+15
-                auto exp_chunk = [&](int ch, const uint32_t (&x)[32], jl::f32x2 nm, jl::f32x2 &lsum) {
-                    uint32_t pk[16];
+                // P = 2^(s*sc - m) for half hh, bf16 pairs into S columns 32hh..32hh+31
+                auto exp_half = [&](int hh, const uint32_t (&x)[64], jl::f32x2 nm, jl::f32x2 &lsum) {
 #pragma unroll
-                    for (int e = 0; e < 16; e++) {
-                        const jl::f32x2 t = jl::fma2(jl::f2(__uint_as_float(x[2 * e]), __uint_as_float(x[2 * e + 1])),
-                                                     sc2, nm);
-                        float t0, t1;
-                        jl::f2_split(t, t0, t1);
-                        const float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
-                        const jl::f32x2 pp = jl::f2(p0, p1);
-                        lsum = jl::add2(lsum, pp);
-                        pk[e] = jl::f2_to_bf16x2(pp);
+                    for (int q = 0; q < 2; q++) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int e = 0; e < 16; e++) {
+                            const int k2 = 32 * q + 2 * e;
+                            const jl::f32x2 t =
+                                jl::fma2(jl::f2(__uint_as_float(x[k2]), __uint_as_float(x[k2 + 1])), sc2, nm);
+                            float t0, t1;
+                            jl::f2_split(t, t0, t1);
+                            const jl::f32x2 pp = jl::f2(fast_exp2(t0), fast_exp2(t1));
+                            lsum = jl::add2(lsum, pp);
+                            pk[e] = jl::f2_to_bf16x2(pp);
+                        }
+                        tmem_st16(tS + 32u * hh + 16u * q, pk);
                     }
-                    tmem_st16(tS + 16u * ch, pk);
                 };
                 if (!(ok = wait_bar_warp(bar(C::B_SFULL + n), v & 1, wc))) break;
                 tc_fence_after();
-                // One pass over the scores, chunk by chunk, against a running
-                // exponent offset m_cur (log2 units).  A chunk whose maximum
-                // exceeds m_cur by more than the threshold raises m_cur by an
-                // integer k (so the chunks already written are rescaled by the
+                // One pass over the scores, 64 columns at a time, against a
+                // running exponent offset m_cur (log2 units).  A half whose
+                // maximum exceeds m_cur by more than the threshold raises m_cur
+                // by an integer k (so the P already written is rescaled by the
                 // exact power of two 2^-k), or sets it when the row had no key
-                // yet.  S is never read again after a chunk's P is written.
+                // yet.  S is never read again after its P is written.
                 float m_cur = m_used;
                 jl::f32x2 lsum = jl::f2(0.f, 0.f);
 #pragma unroll 1
-                for (int ch = 0; ch < kBN / 32; ch++) {
-                    uint32_t x[32];
-                    load_chunk(ch, x);
+                for (int hh = 0; hh < 2; hh++) {
+                    uint32_t x[64];
+                    load_half(hh, x);
                     float cm = -INFINITY;
 #pragma unroll
-                    for (int e = 0; e < 16; e++)
+                    for (int e = 0; e < 32; e++)
                         cm = jl::fmax3(cm, __uint_as_float(x[2 * e]), __uint_as_float(x[2 * e + 1]));
                     cm *= sc;
                     const bool raise = cm > m_cur + kRescaleThreshold;
                     float f = 1.f;
                     if (raise) {
                         if (m_cur == -INFINITY) {
-                            m_cur = cm;  // earlier chunks of this row hold only zeros
+                            m_cur = cm;  // the first half of this row holds only zeros
                         } else {
                             const float k = fminf(ceilf(cm - m_cur), 200.f);
                             m_cur += k;
                             f = ldexpf(1.f, -(int)k);  // exact power of two
                         }
                     }
-                    if (ch > 0 && __any_sync(0xffffffffu, raise && f != 1.f)) {
+                    if (hh > 0 && __any_sync(0xffffffffu, raise && f != 1.f)) {
                         lsum = jl::mul2(lsum, jl::f2(f, f));
-                        tmem_st_wait();  // the P chunks written so far have landed
-                        for (int c2 = 0; c2 < ch; c2++) {
+                        tmem_st_wait();  // the first half's P has landed
+#pragma unroll 1
+                        for (int c2 = 0; c2 < 2; c2++) {
                             uint32_t pk[16];
                             tmem_ld16(tS + 16u * c2, pk);
                             tmem_ld_wait();
@@ -637,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     const float m_off = (m_cur == -INFINITY) ? 0.f : m_cur;
-                    exp_chunk(ch, x, jl::f2(-m_off, -m_off), lsum);
+                    exp_half(hh, x, jl::f2(-m_off, -m_off), lsum);
                 }
                 // the tile moved the row's offset: bring O and l to the new one
                 const bool moved = m_cur != m_used;
