@@ -35,6 +35,19 @@ METRIC = "bifocal prefill attn TFLOP/s @128K (% of BF16 peak); decode µs/token 
 WORKLOAD = dict(B=1, Hq=32, Hkv=8, D=128, S=131072, L_pre=32768, w=4096, theta=1e6, seed=2)
 DECODE_NS = (8192, 32768, 131072)
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+# DRAM bytes (read + write) of one 128K bifocal prefill launch from the ncu
+# launch list in profiles/launches_bench_prefill128k_decode128k.md, valid only
+# for the prefill source it was measured on (first 16 hex digits of its sha256).
+PREFILL_TRAFFIC = {"sha256_16": "23d3ce306acf63e0", "bytes": 221.0e9 + 1.056e9}
+
+
+def prefill_traffic():
+    import hashlib
+
+    path = os.path.join(ROOT, "zero_shot_rope_02_b300", "csrc", "prefill.cu")
+    with open(path, "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    return PREFILL_TRAFFIC["bytes"] if h == PREFILL_TRAFFIC["sha256_16"] else None
 
 
 def prefill_flops(B, Hq, D, S):
@@ -202,7 +215,7 @@ def run_ours(args, rank, world, dev):
         "decode_in_step_us": round(1e3 * sum(decode_ms) / len(decode_ms), 2),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
-                     "traffic": None, "kernel": "prefill_kernel<128>",
+                     "traffic": prefill_traffic(), "kernel": "prefill_kernel<128,2>",
                      "peak_source": f"{peaks_src} bf16 burst"},
         "gpu_launches": 2 * args.steps,
         "clocks": clk.summary(),
