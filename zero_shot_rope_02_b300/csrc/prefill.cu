@@ -371,13 +371,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const WaitCtx wc{p.status, abort_flag};
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int u = blockIdx.x;
-    const int hp = u % p.pairs;
-    u /= p.pairs;
-    const int hk = u % p.Hkv;
-    const int b = u / p.Hkv;
-    const int h0 = hk * p.grp + hp * NH;              // first head of this CTA
-    const int qt = p.n_qtiles - 1 - (int)blockIdx.y;  // longest rows first
+    // blockIdx.x walks (query tile, head pair) with the pair fastest and the
+    // longest rows first; blockIdx.y is (batch, kv head).  Every wave of CTAs
+    // thus works on one kv head, whose K/V (64 MB at 128K) stays in L2.
+    const int hp = (int)blockIdx.x % p.pairs;
+    const int qt = p.n_qtiles - 1 - (int)blockIdx.x / p.pairs;
+    const int hk = (int)blockIdx.y % p.Hkv;
+    const int b = (int)blockIdx.y / p.Hkv;
+    const int h0 = hk * p.grp + hp * NH;  // first head of this CTA
     const int i0 = qt * kBM;
     const int S = p.S, w = p.w, g = p.g;
     Visit vis;
@@ -739,7 +740,7 @@ int launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, 
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, NH>::SMEM);
     if (e != cudaSuccess) return jl::cuda_status(e);
-    dim3 grid((unsigned)(p.B * p.Hkv * p.pairs), (unsigned)p.n_qtiles, 1);
+    dim3 grid((unsigned)(p.pairs * p.n_qtiles), (unsigned)(p.B * p.Hkv), 1);
     kern<<<grid, kThreads, Cfg<D, NH>::SMEM, st>>>(tq, tk, tv, p, pt, rc);
     return jl::cuda_status(cudaGetLastError());
 }
@@ -760,7 +761,7 @@ extern "C" int jl_bifocal_prefill(const void *q, const void *k, const void *v, v
         return JL_ERR_ALIGN;
     if ((long long)B * S * Hq * D > ((long long)1 << 46)) return JL_ERR_OVERFLOW;
     const long long n_qtiles = ((long long)S + kBM - 1) / kBM;
-    if ((long long)B * Hq > 0x7fffffffLL || n_qtiles > 65535) return JL_ERR_OVERFLOW;
+    if ((long long)B * Hkv > 65535 || (long long)Hq * n_qtiles > 0x7fffffffLL) return JL_ERR_OVERFLOW;
     jl::PhaseTable pt;
     if (!jl::make_phase_table(&pt, D, theta)) return JL_ERR_ARG;
     CUtensorMap tq, tk, tv;
