@@ -215,6 +215,16 @@ int jl_debug_grouped_positions(int64_t S, int64_t L_pre, int32_t *out_dev, void 
 int jl_debug_tile_classes(int S, int L_pre, int w, int8_t *out_dev, void *stream);
 
 /*
+ * Debug: exercises the failure path of every bounded device wait.  One warp
+ * waits on an mbarrier that nothing arrives on, with a limit of limit_ns
+ * (1 ns .. 100 ms) instead of the kernels' 2 s; the wait gives up, records
+ * JL_ERR_TIMEOUT in the device status word and the kernel returns normally
+ * (no trap, no hang).  gave_up_dev (device int) receives 1 when the wait gave
+ * up.  Returns JL_OK, JL_ERR_ARG or JL_ERR_CUDA.
+ */
+int jl_debug_wait_timeout(int64_t limit_ns, int *gave_up_dev, void *stream);
+
+/*
  * Debug: read and clear the device status word of the current device
  * (JL_OK, JL_ERR_TIMEOUT or JL_ERR_GUARD).  Synchronises the device; meant
  * for tests, not for the hot path.

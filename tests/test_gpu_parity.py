@@ -81,6 +81,19 @@ def test_tile_classes_match_definition(jl, dev, S, L, w):
     assert np.array_equal(got, _classes_by_definition(S, L, w))
 
 
+def test_bounded_wait_gives_up_and_reports(jl, dev):
+    """A wait whose phase never completes gives up after its limit, sets
+    JL_ERR_TIMEOUT in the status word, and leaves the context usable."""
+    import torch
+
+    assert jl.jl_debug_status() == 0
+    assert jl.jl_debug_wait_timeout(1_000_000) == 1
+    assert jl.jl_debug_status() == jl.JL_ERR_TIMEOUT
+    assert jl.jl_debug_status() == 0  # read-and-clear
+    x = torch.ones(1024, device=dev)
+    assert float(x.sum().item()) == 1024.0
+
+
 # ------------------------------------------------------------------ rope
 @pytest.mark.parametrize("D,pos0,theta", [(128, 0, 1e6), (128, 123457, 1e6), (64, 70000, 1e4),
                                           (16, 5, 500.0), (6, 3, 1e4)])

@@ -31,6 +31,7 @@ EXPORTS = (
     "jl_status_string", "jl_version", "jl_group_factor", "jl_rope_apply", "jl_bifocal_prefill",
     "jl_bifocal_decode_workspace_size", "jl_bifocal_decode", "jl_debug_grouped_positions",
     "jl_debug_tile_classes", "jl_debug_status", "jl_bifocal_decode_noalloc",
+    "jl_debug_wait_timeout",
 )
 
 
@@ -60,6 +61,7 @@ def _load() -> ctypes.CDLL:
         "jl_debug_grouped_positions": (i32, [i64, i64, p, p]),
         "jl_debug_tile_classes": (i32, [i32, i32, i32, p, p]),
         "jl_debug_status": (i32, [ctypes.POINTER(ctypes.c_int)]),
+        "jl_debug_wait_timeout": (i32, [i64, p, p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -229,6 +231,15 @@ def jl_debug_tile_classes(S: int, L_pre: int, w: int, stream=None):
     _check("jl_debug_tile_classes",
            lib.jl_debug_tile_classes(int(S), int(L_pre), int(w), _ptr(out), _stream(stream)))
     return out
+
+
+def jl_debug_wait_timeout(limit_ns: int, stream=None) -> int:
+    """Run the bounded-wait failure probe; returns 1 if the wait gave up."""
+    import torch
+
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _check("jl_debug_wait_timeout", lib.jl_debug_wait_timeout(int(limit_ns), _ptr(flag), _stream(stream)))
+    return int(flag.item())
 
 
 def jl_debug_status() -> int:

@@ -5,6 +5,7 @@
 #include <stdio.h>
 
 #include "jl_common.cuh"
+#include "sm100_ptx.cuh"
 #include "tile_class.cuh"
 
 // Device status word: kernels record JL_ERR_TIMEOUT / JL_ERR_GUARD here
@@ -162,6 +163,25 @@ __global__ void grouped_positions_kernel(int32_t *out, int64_t S, int g)
     if (p < S) out[p] = jl::grouped_pos((int)p, g);
 }
 
+// One warp waits on an mbarrier that nothing ever arrives on, through the
+// same bounded warp-wide wait the attention kernels use, with a short limit:
+// the wait must give up, record JL_ERR_TIMEOUT and let the kernel return.
+__global__ void wait_timeout_kernel(int *status, unsigned long long limit_ns, int *gave_up)
+{
+    __shared__ __align__(8) unsigned long long bar;
+    __shared__ int abort_flag;
+    const uint32_t b = jl::ptx::smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        jl::ptx::mbar_init(b, 1);
+        abort_flag = 0;
+        jl::ptx::fence_mbar_init();
+    }
+    __syncwarp();
+    const jl::ptx::WaitCtx wc{status, &abort_flag, limit_ns};
+    const bool ok = jl::ptx::wait_bar_warp(b, 0, wc);
+    if (threadIdx.x == 0) *gave_up = ok ? 0 : 1;
+}
+
 __global__ void tile_classes_kernel(int8_t *out, int S, int w, int g, int nt)
 {
     int t = blockIdx.x * blockDim.x + threadIdx.x;
@@ -219,6 +239,15 @@ int jl_debug_tile_classes(int S, int L_pre, int w, int8_t *out_dev, void *stream
     int64_t n = (int64_t)nt * nt;
     tile_classes_kernel<<<(unsigned)((n + 255) / 256), 256, 0, (cudaStream_t)stream>>>(out_dev, S, w,
                                                                                       g, nt);
+    return jl::cuda_status(cudaGetLastError());
+}
+
+int jl_debug_wait_timeout(int64_t limit_ns, int *gave_up_dev, void *stream)
+{
+    if (!gave_up_dev || limit_ns < 1 || limit_ns > 100000000) return JL_ERR_ARG;
+    int *st = jl::status_word_ptr();
+    if (!st) return JL_ERR_CUDA;
+    wait_timeout_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(st, (unsigned long long)limit_ns, gave_up_dev);
     return jl::cuda_status(cudaGetLastError());
 }
 

@@ -57,6 +57,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 struct WaitCtx {
     int *status;
     volatile int *abort;
+    unsigned long long limit_ns = kWaitLimitNs;
 };
 
 // Single-thread bounded wait for the phase with the given parity.
@@ -69,7 +70,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Wa
         for (int k = 0; k < 32; k++)
             if (mbar_try_wait(bar, parity)) return true;
         if (*w.abort) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > w.limit_ns) {
             record_status(w.status, JL_ERR_TIMEOUT);
             *w.abort = 1;
             return false;
@@ -90,7 +91,7 @@ __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, con
         int stop = 0;
         if ((threadIdx.x & 31) == 0) {
             if (*w.abort) stop = 1;
-            else if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            else if (globaltimer_ns() - t0 > w.limit_ns) {
                 record_status(w.status, JL_ERR_TIMEOUT);
                 *w.abort = 1;
                 stop = 1;
