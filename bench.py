@@ -407,8 +407,10 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": "Qwen3-8B-shaped bifocal prefill at 128K (bounded row sample)",
-                       **{k_: WORKLOAD[k_] for k_ in ("B", "Hq", "Hkv", "D", "S", "L_pre", "w", "theta")}},
+            "config": {"workload": "Qwen3-8B-shaped bifocal prefill at 128K + decode of the last token",
+                       **{k_: WORKLOAD[k_] for k_ in ("B", "Hq", "Hkv", "D", "S", "L_pre", "w", "theta")},
+                       "g": max(1, -(-WORKLOAD["S"] // WORKLOAD["L_pre"])),
+                       "l2": "inputs larger than L2 (q 1 GiB, k and v 256 MiB each)"},
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
