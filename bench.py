@@ -446,6 +446,56 @@ def replica_value(units_per_rank, ms_per_rank, world):
     return world * units_per_rank / (total_ms * 1e-3), total_ms
 
 
+def run_case(args):
+    """Kernel-only runs for profiling (no JSON line): ``--case prefill`` launches
+    the prefill ``--reps`` times at S=``--S`` (Qwen3-8B head shapes), ``--case
+    decode`` the decode at n=``--n``; prints device time per launch and the
+    host time to enqueue one call."""
+    import torch
+
+    import zero_shot_rope_02_b300 as jl
+    from zero_shot_rope_02_b300 import inputs
+
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    if args.case == "prefill":
+        cfg = dict(WORKLOAD, S=args.S)
+        q, k, v = make_inputs(dev, cfg)
+        out = torch.empty_like(q)
+        lse = torch.empty((1, cfg["Hq"], args.S), dtype=torch.float32, device=dev)
+        L = args.L if args.L > 0 else cfg["L_pre"]
+
+        def call():
+            jl.jl_bifocal_prefill(q, k, v, L, cfg["w"], cfg["theta"], out=out, lse=lse, stream=stream)
+        flops = prefill_flops(1, cfg["Hq"], cfg["D"], args.S)
+    else:
+        n = args.n
+        q = inputs.to_torch_bf16(inputs.normal_bf16_bits((1, 32, 128), 3, 3)).to(dev)
+        k = inputs.to_torch_bf16(inputs.normal_bf16_bits((1, n, 8, 128), 3, 4)).to(dev)
+        v = inputs.to_torch_bf16(inputs.normal_bf16_bits((1, n, 8, 128), 3, 5)).to(dev)
+        ws = torch.zeros(jl.jl_bifocal_decode_workspace_size(1, 32, 8, n, 128), dtype=torch.uint8, device=dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((1, 32), dtype=torch.float32, device=dev)
+        L = args.L if args.L > 0 else 32768
+
+        def call():
+            jl.jl_bifocal_decode(q, k, v, n, L, 4096, 1e6, workspace=ws, out=o, lse=lse, stream=stream)
+        flops = 0.0
+    call()
+    torch.cuda.synchronize(dev)
+    t = time.perf_counter()
+    for _ in range(args.reps):
+        call()
+    host_us = 1e6 * (time.perf_counter() - t) / args.reps
+    torch.cuda.synchronize(dev)
+    ms = time_calls(call, stream, dev, args.reps)
+    line = {"case": args.case, "ms_per_launch": round(ms, 4), "host_enqueue_us": round(host_us, 2),
+            "status": jl.jl_debug_status()}
+    if flops:
+        line["tflops"] = round(flops / (ms * 1e-3) / 1e12, 2)
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", choices=("prefill", "decode"), default=None,

@@ -62,3 +62,15 @@ def test_single_replica_needs_no_process_group():
 
     value, total_ms = bench.replica_value(3.0e12, 200.0, 1)
     assert total_ms == 200.0 and value == pytest.approx(1.5e13)
+
+
+def test_bench_entry_points_resolve():
+    """Every mode bench.py's command line dispatches to exists (the profiling
+    recipes under profiles/ call ``--case``)."""
+    import sys
+
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+
+    for name in ("run_case", "run_reference", "run_ours", "main"):
+        assert callable(getattr(bench, name, None)), name
