@@ -61,6 +61,10 @@ struct Cfg {
     static constexpr int TILE = kBM * D * 2;     // Q / K / V tile bytes
     static constexpr int NK = (D == 128) ? 3 : 4;                     // K ring stages
     static constexpr int NV = (D == 128) ? (NH == 2 ? 2 : 3) : 4;     // V ring stages
+    // a V stage is refilled only after the PV that frees it, and that PV
+    // follows the MMA issuer's wait on GO[v % NK] -- so the V producer's
+    // arrival for tile v lands in that barrier's phase for v only if NV <= NK
+    static_assert(NV <= NK, "V ring deeper than the K ring");
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + NH * TILE;
     static constexpr int OFF_V = OFF_K + NK * TILE;
@@ -68,8 +72,8 @@ struct Cfg {
     static constexpr int BAR_BYTES = 512;
     static constexpr int SMEM = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
     // barrier indices
-    static constexpr int B_QFULL = 0, B_QGFULL = 1, B_QFREE = 2, B_DRAIN = 3, B_KFULL = 4,
-                         B_KEMPTY = B_KFULL + NK, B_KGFULL = B_KEMPTY + NK, B_VFULL = B_KGFULL + NK,
+    static constexpr int B_QFULL = 0, B_K0READY = 1, B_QFREE = 2, B_DRAIN = 3, B_KFULL = 4,
+                         B_KEMPTY = B_KFULL + NK, B_GO = B_KEMPTY + NK, B_VFULL = B_GO + NK,
                          B_VEMPTY = B_VFULL + NV, B_SFULL = B_VEMPTY + NV, B_PFULL = B_SFULL + 2,
                          B_ODONE = B_PFULL + 2, NBAR = B_ODONE + 2;
     static constexpr int OFF_TMEM_SLOT = 448, OFF_ABORT = 452;
@@ -387,13 +391,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(bar(C::B_QFULL), 1);
-        mbar_init(bar(C::B_QGFULL), 128);
+        mbar_init(bar(C::B_K0READY), 128);
         mbar_init(bar(C::B_QFREE), 1);
         mbar_init(bar(C::B_DRAIN), 1);
         for (int s = 0; s < NK; s++) {
             mbar_init(bar(C::B_KFULL + s), 1);
             mbar_init(bar(C::B_KEMPTY + s), 1);
-            mbar_init(bar(C::B_KGFULL + s), 128);
+            // head 0's softmax, the correction warps and the V producer
+            mbar_init(bar(C::B_GO + s), 128 + 128 + 1);
         }
         for (int s = 0; s < NV; s++) {
             mbar_init(bar(C::B_VFULL + s), 1);
@@ -469,6 +474,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_4d(sV + sv * C::TILE + r * C::REGION, &tv, bar(C::B_VFULL + sv), r * 64, hk,
                                 vis.kt(v) * kBN, b);
                 issued = v + 1;
+                // V(v) landed: one of the three arrivals that let tile v's PV go
+                if (!(ok = wait_bar(bar(C::B_VFULL + sv), (v / NV) & 1, wc))) break;
+                mbar_arrive(bar(C::B_GO + v % NK));
             }
             if (!ok) {
                 for (int v = issued - NV < 0 ? 0 : issued - NV; v < issued; v++)
@@ -481,58 +489,50 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, false, false);
             constexpr uint32_t idSG = idesc_f16_f32(kBM, kBN, false, false);
             constexpr uint32_t idPV = idesc_bf16_f32(kBM, D, false, true);
-            bool ok = wait_bar(bar(C::B_QFULL), 0, wc);
-            if (ok && NR > 0) ok = wait_bar(bar(C::B_QGFULL), 0, wc);
-            // waits before the QK of virtual tile v
-            auto prep_qk = [&](int v) -> bool {
-                const int sk = v % NK;
-                if (!wait_bar(bar(C::B_KFULL + sk), (v / NK) & 1, wc)) return false;
-                if (vis.remote(v)) {
-                    if (!wait_bar(bar(C::B_KGFULL + sk), (v / NK) & 1, wc)) return false;
-                } else if (v == NR && NR > 0) {
-                    if (!wait_bar(bar(C::B_QFULL), 1, wc)) return false;  // Q reloaded
-                }
-                tc_fence_after();
-                return true;
-            };
+            // The issuing thread runs at most about one MMA ahead of the tensor
+            // pipe, and every mbarrier wait it makes costs ~200 cycles of pipe
+            // time even when the phase is already complete (the SS MMAs keep
+            // shared memory busy).  So it waits twice per virtual tile: on
+            // GO[v % NK] -- head 0's P(v) written, V(v) landed, K(v+1) landed and
+            // (remote) corrected, Q reloaded before the first exact QK -- and on
+            // head 1's P(v).  The first QK waits on K0READY (Q and K(0) ready).
+            bool ok = wait_bar(bar(C::B_K0READY), 0, wc);
+            tc_fence_after();
+            // S_n = Q_n K^T.  The descriptors are built once per operand tile and
+            // advanced by each k-step's byte offset (>> 4), keeping the issuing
+            // thread's instructions between MMAs to a minimum.
             auto qk_head = [&](int v, int n) {
-                const uint32_t kb = sK + (v % NK) * C::TILE, qb = sQ + n * C::TILE;
+                const uint64_t dk = sdesc_sw128(sK + (v % NK) * C::TILE, 16, 1024);
+                const uint64_t dq = sdesc_sw128(sQ + n * C::TILE, 16, 1024);
                 const uint32_t id = vis.remote(v) ? idSG : idS;
 #pragma unroll
                 for (int k = 0; k < D / 16; k++) {
-                    const uint32_t off = (k >> 2) * C::REGION + (k & 3) * 32;
-                    mma_f16_ss(tmem + 128u * n, sdesc_sw128(qb + off, 16, 1024),
-                               sdesc_sw128(kb + off, 16, 1024), id, k > 0 ? 1u : 0u);
+                    const uint64_t o = (uint64_t)(((k >> 2) * C::REGION + (k & 3) * 32) >> 4);
+                    mma_f16_ss(tmem + 128u * n, dq + o, dk + o, id, k > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(C::B_SFULL + n));
+                if (n == NH - 1) {
+                    mma_commit(bar(C::B_KEMPTY + v % NK));
+                    if (v == NR - 1) mma_commit(bar(C::B_QFREE));
+                }
             };
-            auto finish_qk = [&](int v) {
-                mma_commit(bar(C::B_KEMPTY + v % NK));
-                if (v == NR - 1) mma_commit(bar(C::B_QFREE));
-            };
-            if (ok && (ok = prep_qk(0))) {
+            if (ok)
                 for (int n = 0; n < NH; n++) qk_head(0, n);
-                finish_qk(0);
-            }
             for (int v = 0; ok && v < T; v++) {
                 const int sv = v % NV;
+                const uint64_t dv = sdesc_sw128(sV + sv * C::TILE, C::REGION, 1024);
                 for (int n = 0; n < NH; n++) {
-                    if (!(ok = wait_bar(bar(C::B_PFULL + n), v & 1, wc))) break;
-                    if (n == 0 && !(ok = wait_bar(bar(C::B_VFULL + sv), (v / NV) & 1, wc))) break;
+                    if (n == 0) ok = wait_bar(bar(C::B_GO + v % NK), (v / NK) & 1, wc);
+                    else ok = wait_bar(bar(C::B_PFULL + n), v & 1, wc);
+                    if (!ok) break;
                     tc_fence_after();
-                    const uint32_t vb = sV + sv * C::TILE;
 #pragma unroll
                     for (int k = 0; k < kBN / 16; k++)
                         mma_f16_ts(tmem + 256u + 128u * n, tmem + 128u * n + 8u * k,
-                                   sdesc_sw128(vb + k * 2048, C::REGION, 1024), idPV,
-                                   (v > 0 || k > 0) ? 1u : 0u);
+                                   dv + (uint64_t)((k * 2048) >> 4), idPV, (v > 0 || k > 0) ? 1u : 0u);
                     mma_commit(bar(C::B_ODONE + n));
                     if (n == NH - 1) mma_commit(bar(C::B_VEMPTY + sv));
-                    if (v + 1 < T) {
-                        if (n == 0 && !(ok = prep_qk(v + 1))) break;
-                        qk_head(v + 1, n);
-                        if (n == NH - 1) finish_qk(v + 1);
-                    }
+                    if (v + 1 < T) qk_head(v + 1, n);
                 }
             }
             if (!ok) {
@@ -674,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 l += l0 + l1;
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(bar(C::B_PFULL + n));
+                mbar_arrive(n == 0 ? bar(C::B_GO + v % NK) : bar(C::B_PFULL + n));
             }
             // ------------------------------------------------------------ epilogue
             if (ok) ok = wait_bar_warp(bar(C::B_ODONE + n), (T - 1) & 1, wc);
@@ -704,24 +704,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ correction
-        if (NR > 0) {
-            const int t = threadIdx.x - 256;
-            Corrector<D> cor;
-            cor.init(t, g, pt, rc);
-            bool ok = wait_bar_warp(bar(C::B_QFULL), 0, wc);
-            if (ok) {
+        // Makes K(u) ready for QK(u): waits for it to land and, on a remote
+        // tile, rotates it in place; then arrives on the barrier the MMA issuer
+        // waits on before QK(u) -- K0READY for u = 0 (after correcting Q when
+        // the CTA has a remote phase), else GO[(u-1) % NK]; before the first
+        // exact tile it also waits for the exact Q to be reloaded.  u = T loads
+        // nothing (tile T-1's PV has no QK after it) and only arrives.
+        const int t = threadIdx.x - 256;
+        Corrector<D> cor;
+        if (NR > 0) cor.init(t, g, pt, rc);
+        bool ok = wait_bar_warp(bar(C::B_QFULL), 0, wc);
+        if (ok && NR > 0) {
 #pragma unroll 1
-                for (int n = 0; n < NH; n++) cor.run_q(sQ + n * C::TILE, i0);
-                fence_proxy_async_smem();
-                mbar_arrive(bar(C::B_QGFULL));
+            for (int n = 0; n < NH; n++) cor.run_q(sQ + n * C::TILE, i0);
+        }
+        for (int u = 0; ok && u <= T; u++) {
+            if (u < T) {
+                const int sk = u % NK;
+                if (!(ok = wait_bar_warp(bar(C::B_KFULL + sk), (u / NK) & 1, wc))) break;
+                if (u < NR) cor.run_k(sK + sk * C::TILE, u);
+                if (u == NR && NR > 0 && !(ok = wait_bar_warp(bar(C::B_QFULL), 1, wc))) break;
+                if (u <= NR) fence_proxy_async_smem();
             }
-            for (int v = 0; ok && v < NR; v++) {
-                const int sk = v % NK;
-                if (!(ok = wait_bar_warp(bar(C::B_KFULL + sk), (v / NK) & 1, wc))) break;
-                cor.run_k(sK + sk * C::TILE, v);
-                fence_proxy_async_smem();
-                mbar_arrive(bar(C::B_KGFULL + sk));
-            }
+            // An arrival for tile u-1 must not land in GO's phase for tile
+            // u-1-NK.  For u < T the landing of K(u) orders it (the stage is
+            // refilled only after QK(u-NK), which follows the issuer's wait on
+            // that phase); the last one has no K to wait for, so it waits for
+            // that phase itself.
+            if (u == T && T - 1 >= NK &&
+                !(ok = wait_bar_warp(bar(C::B_GO + (T - 1) % NK), (((T - 1) / NK) & 1) ^ 1, wc)))
+                break;
+            mbar_arrive(u == 0 ? bar(C::B_K0READY) : bar(C::B_GO + (u - 1) % NK));
         }
     }
 
