@@ -54,6 +54,12 @@ def prefill_flops(B, Hq, D, S):
     return 2.0 * B * Hq * D * S * S
 
 
+def chunk_prefill_flops(B, Hq, D, S_new, n_past):
+    """Same convention as prefill_flops (4*D FLOP per (query, key) pair, the
+    causal half of the new tokens' own block): S_new*n_past + S_new^2/2 pairs."""
+    return 2.0 * B * Hq * D * (2.0 * S_new * n_past + S_new * S_new)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -197,6 +203,19 @@ def run_ours(args, rank, world, dev):
     plain_ms = time_calls(lambda: jl.jl_bifocal_prefill(q, k, v, S, w, theta, out=out, lse=lse,
                                                         stream=stream), stream, dev, reps=max(3, args.steps))
     decode = decode_sweep(jl, dev, stream, peaks)
+    # chunked prefill: the last 8K tokens of the same context over the cache of
+    # the first 120K (same k / v buffers as the cache), s = S as above
+    S_new = 8192
+    n_past = S - S_new
+    qc = q[:, n_past:].contiguous()
+    outc = torch.empty_like(qc)
+    lsec = torch.empty((B, Hq, S_new), dtype=torch.float32, device=dev)
+    chunk_ms = time_calls(lambda: jl.jl_bifocal_prefill_chunk(qc, k, v, n_past, L, w, theta, out=outc,
+                                                              lse=lsec, stream=stream),
+                          stream, dev, reps=max(3, args.steps))
+    chunk_flops = chunk_prefill_flops(B, Hq, D, S_new, n_past)
+    if jl.jl_debug_status() != 0:
+        raise RuntimeError("device status word set by the chunk run")
 
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
@@ -212,6 +231,9 @@ def run_ours(args, rank, world, dev):
         "plain_rope": {"tflops": round(flops / (plain_ms * 1e-3) / 1e12, 2), "ms": round(plain_ms, 3),
                        "bifocal_overhead": round(avg_prefill_ms / plain_ms - 1.0, 4)},
         "decode": decode,
+        "chunk": {"S_new": S_new, "n_past": n_past, "ms": round(chunk_ms, 3),
+                  "tflops": round(chunk_flops / (chunk_ms * 1e-3) / 1e12, 2),
+                  "frac_of_bf16_peak": round(chunk_flops / (chunk_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)},
         "decode_in_step_us": round(1e3 * sum(decode_ms) / len(decode_ms), 2),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),

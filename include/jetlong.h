@@ -135,6 +135,28 @@ int jl_bifocal_prefill(const void *q, const void *k, const void *v, void *out, f
                        double theta, void *stream);
 
 /*
+ * Bifocal prefill of a chunk over an existing cache: S_new new tokens at
+ * positions n_past..n_past+S_new-1 attend to every key at positions
+ * 0..n_past+S_new-1 (the cached tokens and themselves, causally).  This is
+ * the prefill step the pages place before generation, run in pieces; s =
+ * n_past + S_new sets g = g(s, L_pre), so a chunk scores exactly the rows a
+ * full prefill of length s would give those positions.  The caller has
+ * already written the chunk's exact-RoPE K/V into cache rows n_past..n_past+
+ * S_new-1; the cache keeps original positions and is never rewritten.
+ *   q        device bf16 [B, S_new, Hq, D], exact RoPE at n_past..n_past+S_new-1
+ *   k_cache, v_cache  device bf16 [B, n_cap, Hkv, D]; rows 0..n_past+S_new-1
+ *            are read, the rest of the capacity never (it may hold anything)
+ *   out      device bf16 [B, S_new, Hq, D];  lse device fp32 [B, Hq, S_new]
+ *   S_new >= 1, n_past >= 0, n_past + S_new <= n_cap, other arguments as in
+ *   jl_bifocal_prefill (which is this call with n_past = 0, n_cap = S).
+ * Returns JL_OK, JL_ERR_ARG, JL_ERR_ALIGN, JL_ERR_UNSUPPORTED, JL_ERR_OVERFLOW
+ * or JL_ERR_CUDA.
+ */
+int jl_bifocal_prefill_chunk(const void *q, const void *k_cache, const void *v_cache, void *out,
+                             float *lse, int B, int Hq, int Hkv, int S_new, int n_past, int n_cap,
+                             int D, int L_pre, int w, double theta, void *stream);
+
+/*
  * Workspace bytes jl_bifocal_decode needs for these sizes (split-KV partial
  * statistics and one arrival counter per (batch, kv head)).  The value does
  * not grow with n: a workspace sized once serves every cache length for the
@@ -150,7 +172,8 @@ size_t jl_bifocal_decode_workspace_size(int B, int Hq, int Hkv, int n, int D);
  * and the cache holds positions 0..n-1 including it; g = g(n, L_pre); key j
  * is exact when n-1-j < w, aliased otherwise.
  *   q        device bf16 [B, Hq, D], exact RoPE at position n-1
- *   k_cache, v_cache  device bf16 [B, n_cap, Hkv, D]; rows 0..n-1 are read
+ *   k_cache, v_cache  device bf16 [B, n_cap, Hkv, D]; rows 0..n-1 are read,
+ *            the rest of the capacity never (it may hold anything)
  *   out      device bf16 [B, Hq, D];  lse device fp32 [B, Hq]
  *   n        1 <= n <= n_cap (current length), n_cap the cache capacity
  *   workspace  device, >= jl_bifocal_decode_workspace_size() bytes, 16-byte

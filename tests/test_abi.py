@@ -27,6 +27,15 @@ def test_every_declared_symbol_is_exported(jl):
     assert set(names) == set(jl.EXPORTS)
 
 
+def test_every_entry_point_is_reachable_from_the_package(jl):
+    """The package forwards every wrapped C entry point (its names are lazy)."""
+    import zero_shot_rope_02_b300 as pkg
+
+    for name in jl.EXPORTS:
+        if hasattr(jl, name):  # a Python wrapper of that name exists
+            assert getattr(pkg, name) is getattr(jl, name), name
+
+
 def test_version_and_status_strings(jl):
     assert jl.jl_version().count(".") == 2
     for code in range(-8, 1):
@@ -74,6 +83,24 @@ def test_prefill_argument_checks(jl):
     for name in ("q", "k", "v", "out", "lse"):
         assert _prefill(jl, **{name: BAD}) == jl.JL_ERR_ALIGN, name
     assert _prefill(jl, B=1 << 20, Hq=1 << 10, Hkv=1, S=1 << 20) == jl.JL_ERR_OVERFLOW
+
+
+def _chunk(jl, q=GOOD, k=GOOD, v=GOOD, out=GOOD, lse=GOOD, B=1, Hq=32, Hkv=8, S_new=64, n_past=100,
+           n_cap=164, D=128, L=4096, w=128, theta=1e6):
+    return jl.lib.jl_bifocal_prefill_chunk(q, k, v, out, lse, B, Hq, Hkv, S_new, n_past, n_cap, D, L, w,
+                                           theta, None)
+
+
+def test_prefill_chunk_argument_checks(jl):
+    """Rejected before any launch (no GPU needed)."""
+    assert _chunk(jl, D=96) == jl.JL_ERR_UNSUPPORTED
+    for kw in ({"S_new": 0}, {"n_past": -1}, {"n_cap": 163}, {"w": 0}, {"L": 0}, {"theta": 0.0},
+               {"Hq": 3, "Hkv": 2}):
+        assert _chunk(jl, **kw) == jl.JL_ERR_ARG, kw
+    assert _chunk(jl, k=None) == jl.JL_ERR_ARG
+    for name in ("q", "k", "v", "out", "lse"):
+        assert _chunk(jl, **{name: BAD}) == jl.JL_ERR_ALIGN, name
+    assert _chunk(jl, n_past=(1 << 31) - 10, n_cap=(1 << 31) - 1) == jl.JL_ERR_OVERFLOW
 
 
 def _decode(jl, q=GOOD, k=GOOD, v=GOOD, out=GOOD, lse=GOOD, B=1, Hq=32, Hkv=8, n=100, n_cap=100,

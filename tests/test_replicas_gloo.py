@@ -74,3 +74,16 @@ def test_bench_entry_points_resolve():
 
     for name in ("run_case", "run_reference", "run_ours", "main"):
         assert callable(getattr(bench, name, None)), name
+
+
+def test_chunk_flop_convention_adds_up_to_the_full_prefill():
+    """Chunks of one context count exactly the full prefill's work."""
+    import sys
+
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+
+    full = bench.prefill_flops(1, 32, 128, 131072)
+    assert bench.chunk_prefill_flops(1, 32, 128, 131072, 0) == full
+    parts = [(0, 50000), (50000, 8192), (58192, 131072 - 58192)]
+    assert sum(bench.chunk_prefill_flops(1, 32, 128, s_new, n_past) for n_past, s_new in parts) == full

@@ -10,7 +10,7 @@ _BINDING_NAMES = (
     "EXPORTS", "JetLongError", "LIB_PATH", "jl_bifocal_decode", "jl_bifocal_decode_workspace_size",
     "jl_bifocal_prefill", "jl_debug_grouped_positions", "jl_debug_status", "jl_debug_tile_classes",
     "jl_group_factor", "jl_rope_apply", "jl_version", "lib", "status_string",
-    "jl_bifocal_decode_noalloc", "jl_debug_wait_timeout",
+    "jl_bifocal_decode_noalloc", "jl_debug_wait_timeout", "jl_bifocal_prefill_chunk",
 )
 
 __all__ = list(_BINDING_NAMES)

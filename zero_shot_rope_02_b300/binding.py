@@ -31,7 +31,7 @@ EXPORTS = (
     "jl_status_string", "jl_version", "jl_group_factor", "jl_rope_apply", "jl_bifocal_prefill",
     "jl_bifocal_decode_workspace_size", "jl_bifocal_decode", "jl_debug_grouped_positions",
     "jl_debug_tile_classes", "jl_debug_status", "jl_bifocal_decode_noalloc",
-    "jl_debug_wait_timeout",
+    "jl_debug_wait_timeout", "jl_bifocal_prefill_chunk",
 )
 
 
@@ -53,6 +53,8 @@ def _load() -> ctypes.CDLL:
         "jl_group_factor": (i32, [i64, i64, ctypes.POINTER(ctypes.c_int32)]),
         "jl_rope_apply": (i32, [p, i32, i32, i32, i32, i64, dbl, p]),
         "jl_bifocal_prefill": (i32, [p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, dbl, p]),
+        "jl_bifocal_prefill_chunk": (i32, [p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+                                           dbl, p]),
         "jl_bifocal_decode_workspace_size": (sz, [i32, i32, i32, i32, i32]),
         "jl_bifocal_decode": (i32, [p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, i32, dbl,
                                     p, sz, p]),
@@ -149,6 +151,33 @@ def jl_bifocal_prefill(q, k, v, L_pre: int, w: int, theta: float, out=None, lse=
     _check("jl_bifocal_prefill",
            lib.jl_bifocal_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, S, D,
                                   int(L_pre), int(w), float(theta), _stream(stream)))
+    return out, lse
+
+
+def jl_bifocal_prefill_chunk(q, k_cache, v_cache, n_past: int, L_pre: int, w: int, theta: float,
+                             out=None, lse=None, stream=None):
+    """Bifocal prefill of S_new tokens at positions n_past..n_past+S_new-1 over
+    the cache.  q [B,S_new,Hq,D]; caches [B,n_cap,Hkv,D] bf16 (exact RoPE),
+    rows 0..n_past+S_new-1 valid.  Returns (out bf16 [B,S_new,Hq,D],
+    lse fp32 [B,Hq,S_new])."""
+    import torch
+
+    for t, nm in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, nm)
+    B, S_new, Hq, D = q.shape
+    _, n_cap, Hkv, Dk = k_cache.shape
+    if Dk != D or v_cache.shape != k_cache.shape or k_cache.shape[0] != B:
+        raise ValueError("caches must be [B, n_cap, Hkv, D] matching q")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, S_new), dtype=torch.float32, device=q.device)
+    _need(out, torch.bfloat16, "out")
+    _need(lse, torch.float32, "lse")
+    _check("jl_bifocal_prefill_chunk",
+           lib.jl_bifocal_prefill_chunk(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse), B,
+                                        Hq, Hkv, S_new, int(n_past), n_cap, D, int(L_pre), int(w),
+                                        float(theta), _stream(stream)))
     return out, lse
 
 

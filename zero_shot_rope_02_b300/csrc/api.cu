@@ -74,11 +74,11 @@ static EncodeTiledFn encode_fn()
 namespace {
 struct MapKey {
     const void *base;
-    int B, S, H, D, box_d, box_rows, sw;
+    int B, S, S_cap, H, D, box_d, box_rows, sw;
     bool operator==(const MapKey &o) const
     {
-        return base == o.base && B == o.B && S == o.S && H == o.H && D == o.D && box_d == o.box_d &&
-               box_rows == o.box_rows && sw == o.sw;
+        return base == o.base && B == o.B && S == o.S && S_cap == o.S_cap && H == o.H && D == o.D &&
+               box_d == o.box_d && box_rows == o.box_rows && sw == o.sw;
     }
 };
 struct MapCache {
@@ -89,20 +89,20 @@ struct MapCache {
 };
 }  // namespace
 
-static bool encode_bshd_map(CUtensorMap *m, const void *base, int B, int S, int H, int D, int box_d,
-                            int box_rows, bool swizzle128);
+static bool encode_bshd_map(CUtensorMap *m, const void *base, int B, int S, int S_cap, int H, int D,
+                            int box_d, int box_rows, bool swizzle128);
 
-bool make_bshd_map(CUtensorMap *m, const void *base, int B, int S, int H, int D, int box_d,
-                   int box_rows, bool swizzle128)
+bool make_bshd_map(CUtensorMap *m, const void *base, int B, int S, int S_cap, int H, int D,
+                   int box_d, int box_rows, bool swizzle128)
 {
     thread_local MapCache cache;
-    const MapKey k{base, B, S, H, D, box_d, box_rows, swizzle128 ? 1 : 0};
+    const MapKey k{base, B, S, S_cap, H, D, box_d, box_rows, swizzle128 ? 1 : 0};
     for (int i = 0; i < cache.used; i++)
         if (cache.key[i] == k) {
             *m = cache.map[i];
             return true;
         }
-    if (!encode_bshd_map(m, base, B, S, H, D, box_d, box_rows, swizzle128)) return false;
+    if (!encode_bshd_map(m, base, B, S, S_cap, H, D, box_d, box_rows, swizzle128)) return false;
     cache.key[cache.next] = k;
     cache.map[cache.next] = *m;
     cache.next = (cache.next + 1) % MapCache::N;
@@ -110,14 +110,14 @@ bool make_bshd_map(CUtensorMap *m, const void *base, int B, int S, int H, int D,
     return true;
 }
 
-static bool encode_bshd_map(CUtensorMap *m, const void *base, int B, int S, int H, int D, int box_d,
-                            int box_rows, bool swizzle128)
+static bool encode_bshd_map(CUtensorMap *m, const void *base, int B, int S, int S_cap, int H, int D,
+                            int box_d, int box_rows, bool swizzle128)
 {
     EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
+    if (!fn || S < 1 || S > S_cap) return false;
     cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
-    // byte strides of dims 1..3 (H, S, B)
-    cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)S * H * D * 2};
+    // byte strides of dims 1..3 (H, S, B); a batch entry spans S_cap rows
+    cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)S_cap * H * D * 2};
     cuuint32_t box[4] = {(cuuint32_t)box_d, 1, (cuuint32_t)box_rows, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,

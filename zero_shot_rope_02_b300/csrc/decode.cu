@@ -514,8 +514,10 @@ int launch(const DecodeArgs &a, int B, int n_cap, const void *k_cache, const voi
         attr_set[dev] = true;
     }
     CUtensorMap tk, tv;
-    if (!jl::make_bshd_map(&tk, k_cache, B, n_cap, a.Hkv, D, D, kKB, false) ||
-        !jl::make_bshd_map(&tv, v_cache, B, n_cap, a.Hkv, D, D, kKB, false))
+    // only rows [0, n) are mapped: the block that holds key n-1 reads zeros past
+    // it, never the cache's unused capacity (0 * NaN would poison P.V)
+    if (!jl::make_bshd_map(&tk, k_cache, B, a.n, n_cap, a.Hkv, D, D, kKB, false) ||
+        !jl::make_bshd_map(&tv, v_cache, B, a.n, n_cap, a.Hkv, D, D, kKB, false))
         return JL_ERR_CUDA;
     dim3 grid(a.splits, a.Hkv, B);
     kern<<<grid, kThreads, C::SMEM, st>>>(tk, tv, a, pt, rot);

@@ -29,11 +29,14 @@ struct PhaseTable {
 // of the "local RoPE-faithful window").  Returns false on bad arguments.
 bool make_phase_table(PhaseTable *t, int D, double theta);
 
-// Host: TMA tensor map over a bf16 [B, S, H, D] tensor viewed as the 4-D
-// tensor {D, H, S, B}; box {box_d, 1, box_rows, 1}; 128-byte swizzle or none;
-// zero fill outside the tensor.  False if the driver refuses it.
-bool make_bshd_map(CUtensorMap *m, const void *base, int B, int S, int H, int D, int box_d,
-                   int box_rows, bool swizzle128);
+// Host: TMA tensor map over a bf16 [B, S_cap, H, D] tensor of which rows
+// [0, S) of every batch entry are mapped, viewed as the 4-D tensor {D, H, S,
+// B} (batch stride S_cap rows); box {box_d, 1, box_rows, 1}; 128-byte swizzle
+// or none.  Loads outside the mapped rows read zeros, so rows at or past S
+// (a cache's unused capacity, whatever it holds) never reach a kernel.
+// False if the driver refuses it.
+bool make_bshd_map(CUtensorMap *m, const void *base, int B, int S, int S_cap, int H, int D,
+                   int box_d, int box_rows, bool swizzle128);
 
 // Host: cos / sin of the angle offset * theta_d, from the same exact
 // fixed-point phase the device uses, evaluated in double precision.

@@ -82,10 +82,12 @@ struct Cfg {
 };
 
 struct Params {
-    __nv_bfloat16 *out;  // [B, S, Hq, D]
-    float *lse;          // [B, Hq, S]
+    __nv_bfloat16 *out;  // [B, Sq, Hq, D]
+    float *lse;          // [B, Hq, Sq]
     int *status;
-    int B, Hq, Hkv, S, w, g, grp, n_qtiles, pairs;  // pairs = grp / NH
+    // S: keys (positions 0..S-1, the length that sets g); the Sq query rows sit
+    // at positions pos0..pos0+Sq-1 = S-Sq..S-1 (pos0 = 0, Sq = S: full prefill)
+    int B, Hq, Hkv, S, Sq, pos0, w, g, grp, n_qtiles, pairs;  // pairs = grp / NH
     float scale_log2;    // tau * log2(e)
 };
 
@@ -330,10 +332,12 @@ struct Corrector {
 struct Visit {
     int nr, kb, T;
 
-    __device__ void init(int i0, int qt, int S, int w, int g)
+    // query rows from absolute position i0; kt_last = the last key tile any of
+    // them reaches (the diagonal tile)
+    __device__ void init(int i0, int kt_last, int S, int w, int g)
     {
         // first kt whose class is not remote; first kt whose class is exact
-        int lo = 0, hi = qt;  // class(qt) is never remote (distance 0 < w)
+        int lo = 0, hi = kt_last;  // class(kt_last) is never remote (distance 0 < w)
         while (lo < hi) {
             int mid = (lo + hi) >> 1;
             if (jl::tile_class(i0, mid * kBN, kBM, kBN, S, w, g) == jl::kTileRemote) lo = mid + 1;
@@ -341,14 +345,14 @@ struct Visit {
         }
         kb = lo;
         lo = kb;
-        hi = qt + 1;
+        hi = kt_last + 1;
         while (lo < hi) {
             int mid = (lo + hi) >> 1;
             if (jl::tile_class(i0, mid * kBN, kBM, kBN, S, w, g) == jl::kTileExact) hi = mid;
             else lo = mid + 1;
         }
         nr = lo;  // tiles [0, nr) have a remote part
-        T = nr + (qt + 1 - kb);
+        T = nr + (kt_last + 1 - kb);
     }
 
     __device__ __forceinline__ int kt(int v) const { return v < nr ? v : kb + (v - nr); }
@@ -383,10 +387,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int hk = (int)blockIdx.y % p.Hkv;
     const int b = (int)blockIdx.y / p.Hkv;
     const int h0 = hk * p.grp + hp * NH;  // first head of this CTA
-    const int i0 = qt * kBM;
+    const int q_row0 = qt * kBM;   // first row of the tile in q / out / lse
+    const int i0 = p.pos0 + q_row0;  // its position
     const int S = p.S, w = p.w, g = p.g;
     Visit vis;
-    vis.init(i0, qt, S, w, g);
+    vis.init(i0, (min(i0 + kBM, S) - 1) / kBN, S, w, g);
     const int T = vis.T, NR = vis.nr;
 
     if (threadIdx.x == 0) {
@@ -433,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int r = 0; r < C::NREG; r++)
                         tma_load_4d(sQ + n * C::TILE + r * C::REGION, &tq, bar(C::B_QFULL), r * 64,
-                                    h0 + n, i0, b);
+                                    h0 + n, q_row0, b);
             };
             load_q();
             int issued = 0;
@@ -681,7 +686,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok) {
                 tc_fence_after();
                 const float inv_l = 1.f / l;
-                __nv_bfloat16 *orow = p.out + (((size_t)b * S + i) * p.Hq + h) * D;
+                const int il = i - p.pos0;  // row in out / lse (valid while i < S)
+                __nv_bfloat16 *orow = p.out + (((size_t)b * p.Sq + il) * p.Hq + h) * D;
 #pragma unroll 1
                 for (int ch = 0; ch < D / 32; ch++) {
                     uint32_t o[32];
@@ -699,7 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
                     }
                 }
-                if (i < S) p.lse[((size_t)b * p.Hq + h) * S + i] = (m_used + log2f(l)) * kLn2;
+                if (i < S) p.lse[((size_t)b * p.Hq + h) * p.Sq + il] = (m_used + log2f(l)) * kLn2;
             }
         }
     } else {
@@ -760,27 +766,35 @@ int launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, 
 
 }  // namespace
 
-extern "C" int jl_bifocal_prefill(const void *q, const void *k, const void *v, void *out, float *lse,
-                                  int B, int Hq, int Hkv, int S, int D, int L_pre, int w,
-                                  double theta, void *stream)
+// Prefill of Sq queries at positions n_past..n_past+Sq-1 over the keys at
+// positions 0..n_past+Sq-1 (k / v: [B, n_cap, Hkv, D], rows past the keys
+// are never read), s = n_past + Sq.
+static int prefill_impl(const void *q, const void *k, const void *v, void *out, float *lse, int B, int Hq,
+                 int Hkv, int Sq, int n_past, int n_cap, int D, int L_pre, int w, double theta,
+                 void *stream)
 {
     if (!q || !k || !v || !out || !lse) return JL_ERR_ARG;
-    if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || L_pre < 1 || w < 1 || !(theta > 0.0) ||
-        Hq % Hkv != 0)
+    if (B < 1 || Hq < 1 || Hkv < 1 || Sq < 1 || n_past < 0 || L_pre < 1 || w < 1 ||
+        !(theta > 0.0) || Hq % Hkv != 0)
         return JL_ERR_ARG;
+    if ((long long)n_past + Sq > 0x7fffffffLL) return JL_ERR_OVERFLOW;
+    const int S = n_past + Sq;
+    if (n_cap < S) return JL_ERR_ARG;
     if (D != 64 && D != 128) return JL_ERR_UNSUPPORTED;
     if (!jl::aligned16(q) || !jl::aligned16(k) || !jl::aligned16(v) || !jl::aligned16(out) ||
         !jl::aligned16(lse))
         return JL_ERR_ALIGN;
-    if ((long long)B * S * Hq * D > ((long long)1 << 46)) return JL_ERR_OVERFLOW;
-    const long long n_qtiles = ((long long)S + kBM - 1) / kBM;
+    if ((long long)B * Sq * Hq * D > ((long long)1 << 46) ||
+        (long long)B * n_cap * Hkv * D > ((long long)1 << 46))
+        return JL_ERR_OVERFLOW;
+    const long long n_qtiles = ((long long)Sq + kBM - 1) / kBM;
     if ((long long)B * Hkv > 65535 || (long long)Hq * n_qtiles > 0x7fffffffLL) return JL_ERR_OVERFLOW;
     jl::PhaseTable pt;
     if (!jl::make_phase_table(&pt, D, theta)) return JL_ERR_ARG;
     CUtensorMap tq, tk, tv;
-    if (!jl::make_bshd_map(&tq, q, B, S, Hq, D, 64, 128, true) ||
-        !jl::make_bshd_map(&tk, k, B, S, Hkv, D, 64, 128, true) ||
-        !jl::make_bshd_map(&tv, v, B, S, Hkv, D, 64, 128, true))
+    if (!jl::make_bshd_map(&tq, q, B, Sq, Sq, Hq, D, 64, 128, true) ||
+        !jl::make_bshd_map(&tk, k, B, S, n_cap, Hkv, D, 64, 128, true) ||
+        !jl::make_bshd_map(&tv, v, B, S, n_cap, Hkv, D, 64, 128, true))
         return JL_ERR_CUDA;
     Params p;
     p.out = (__nv_bfloat16 *)out;
@@ -790,6 +804,8 @@ extern "C" int jl_bifocal_prefill(const void *q, const void *k, const void *v, v
     p.Hq = Hq;
     p.Hkv = Hkv;
     p.S = S;
+    p.Sq = Sq;
+    p.pos0 = n_past;
     p.w = w;
     p.g = (int)jl::group_factor_host(S, L_pre);
     p.grp = Hq / Hkv;
@@ -816,4 +832,20 @@ extern "C" int jl_bifocal_prefill(const void *q, const void *k, const void *v, v
     if (D == 128)
         return nh == 2 ? launch<128, 2>(tq, tk, tv, p, pt, rc, st) : launch<128, 1>(tq, tk, tv, p, pt, rc, st);
     return nh == 2 ? launch<64, 2>(tq, tk, tv, p, pt, rc, st) : launch<64, 1>(tq, tk, tv, p, pt, rc, st);
+}
+
+extern "C" int jl_bifocal_prefill(const void *q, const void *k, const void *v, void *out, float *lse,
+                                  int B, int Hq, int Hkv, int S, int D, int L_pre, int w,
+                                  double theta, void *stream)
+{
+    return prefill_impl(q, k, v, out, lse, B, Hq, Hkv, S, 0, S, D, L_pre, w, theta, stream);
+}
+
+extern "C" int jl_bifocal_prefill_chunk(const void *q, const void *k_cache, const void *v_cache,
+                                        void *out, float *lse, int B, int Hq, int Hkv, int S_new,
+                                        int n_past, int n_cap, int D, int L_pre, int w, double theta,
+                                        void *stream)
+{
+    return prefill_impl(q, k_cache, v_cache, out, lse, B, Hq, Hkv, S_new, n_past, n_cap, D, L_pre, w,
+                        theta, stream);
 }
