@@ -214,6 +214,7 @@ def run_ours(args, rank, world, dev):
                                                               lse=lsec, stream=stream),
                           stream, dev, reps=max(3, args.steps))
     chunk_flops = chunk_prefill_flops(B, Hq, D, S_new, n_past)
+    paged = paged_decode(jl, dev, stream, peaks, args)
     if jl.jl_debug_status() != 0:
         raise RuntimeError("device status word set by the chunk run")
 
@@ -231,6 +232,7 @@ def run_ours(args, rank, world, dev):
         "plain_rope": {"tflops": round(flops / (plain_ms * 1e-3) / 1e12, 2), "ms": round(plain_ms, 3),
                        "bifocal_overhead": round(avg_prefill_ms / plain_ms - 1.0, 4)},
         "decode": decode,
+        "paged_decode": paged,
         "chunk": {"S_new": S_new, "n_past": n_past, "ms": round(chunk_ms, 3),
                   "tflops": round(chunk_flops / (chunk_ms * 1e-3) / 1e12, 2),
                   "frac_of_bf16_peak": round(chunk_flops / (chunk_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)},
@@ -247,6 +249,47 @@ def run_ours(args, rank, world, dev):
     if rank == 0 and not args.no_cpu:
         res["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     return res
+
+
+def paged_decode(jl, dev, stream, peaks, args):
+    """One call decoding four sequences of their own lengths (and own g) over
+    a paged cache: 64-key pages of one pool, in shuffled order."""
+    import numpy as np
+    import torch
+
+    from zero_shot_rope_02_b300 import inputs
+
+    lens = [131072, 65536, 32768, 8192]
+    Hq, Hkv, D, P, L, w = 32, 8, 128, 64, 32768, 4096
+    B = len(lens)
+    pages_per = [n // P for n in lens]
+    num_pages = sum(pages_per)
+    perm = np.random.default_rng(7).permutation(num_pages).astype(np.int32)
+    table = np.zeros((B, max(pages_per)), dtype=np.int32)
+    o = 0
+    for b, k in enumerate(pages_per):
+        table[b, :k] = perm[o:o + k]
+        o += k
+    kp = inputs.to_torch_bf16(inputs.normal_bf16_bits((num_pages, P, Hkv, D), 8, 4)).to(dev)
+    vp = inputs.to_torch_bf16(inputs.normal_bf16_bits((num_pages, P, Hkv, D), 8, 5)).to(dev)
+    q = inputs.to_torch_bf16(inputs.normal_bf16_bits((B, Hq, D), 8, 3)).to(dev)
+    table_d = torch.from_numpy(table).to(dev)
+    lens_d = torch.tensor(lens, dtype=torch.int32, device=dev)
+    ws = torch.zeros(max(16, jl.jl_bifocal_decode_paged_workspace_size(B, Hq, Hkv, max(lens), D)),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    us = 1e3 * time_calls(lambda: jl.jl_bifocal_decode_paged(q, kp, vp, table_d, lens_d, max(lens), L, w,
+                                                             1e6, workspace=ws, out=out, lse=lse,
+                                                             stream=stream),
+                          stream, dev, reps=20)
+    if jl.jl_debug_status() != 0:
+        raise RuntimeError("device status word set by the paged decode")
+    nbytes = sum(lens) * Hkv * D * 2 * 2  # K and V rows of every sequence
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"lens": lens, "page_size": P, "g": [jl.jl_group_factor(n, L) for n in lens],
+            "us_per_call": round(us, 2), "gbs": round(gbs, 1),
+            "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4), "timing": "eager; K and V pools 486 MB each, > 2x L2"}
 
 
 def time_calls(fn, stream, dev, reps):

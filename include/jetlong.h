@@ -188,6 +188,43 @@ int jl_bifocal_decode(const void *q, const void *k_cache, const void *v_cache, v
                       int w, double theta, void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * Bifocal decode of a batch of sequences of different lengths over a paged
+ * KV cache: sequence b has n_b = seq_lens[b] tokens, its query is the token at
+ * position n_b - 1, and it sets its own g = g(n_b, L_pre) -- the group factor
+ * follows each sequence's current length (ResearchPod summary: "every
+ * length").  Its keys live in fixed-size pages of one pool: page p of
+ * sequence b (positions p*page_size .. p*page_size + page_size - 1) is pool
+ * page block_table[b][p].
+ *   q        device bf16 [B, Hq, D], exact RoPE at each sequence's position n_b - 1
+ *   k_pages, v_pages  device bf16 [num_pages, page_size, Hkv, D], exact RoPE
+ *   block_table  device int32 [B, max_pages]; entries past a sequence's last
+ *            page are never read; an id outside [0, num_pages) reads zeros
+ *   seq_lens device int32 [B], 1 <= n_b <= max_n; a length outside that range
+ *            is clamped into it and reported as JL_ERR_GUARD in the device
+ *            status word (the call never reads past the table or the plan)
+ *   out      device bf16 [B, Hq, D];  lse device fp32 [B, Hq]
+ *   page_size  a multiple of 64 (the kernel's key block); max_pages * page_size
+ *            >= max_n (host: the longest sequence, sizes the split plan)
+ *   workspace  as for jl_bifocal_decode, at least
+ *            jl_bifocal_decode_paged_workspace_size(B, Hq, Hkv, max_n, D) bytes
+ * Rows of a sequence's last page past n_b are never used, whatever they hold.
+ * Returns JL_OK, JL_ERR_ARG, JL_ERR_ALIGN, JL_ERR_UNSUPPORTED, JL_ERR_OVERFLOW,
+ * JL_ERR_WORKSPACE or JL_ERR_CUDA.
+ */
+/*
+ * Workspace bytes jl_bifocal_decode_paged needs: its split plan is sized for
+ * the longest sequence (max_n) alone, since a batch may hold one long and many
+ * short sequences.  0 on bad sizes.
+ */
+size_t jl_bifocal_decode_paged_workspace_size(int B, int Hq, int Hkv, int max_n, int D);
+
+int jl_bifocal_decode_paged(const void *q, const void *k_pages, const void *v_pages,
+                            const int32_t *block_table, const int32_t *seq_lens, void *out,
+                            float *lse, int B, int Hq, int Hkv, int D, int page_size, int num_pages,
+                            int max_pages, int max_n, int L_pre, int w, double theta,
+                            void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * Size of the fixed device scratch behind jl_bifocal_decode_noalloc: 8 MiB,
  * enough for B * Hq * splits * (D + 2) * 4 bytes of split partials plus the
  * arrival counters (for example B = 1, Hq = 32, D = 128 at any cache length).

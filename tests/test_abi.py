@@ -125,6 +125,28 @@ def test_decode_argument_checks(jl):
     assert _decode(jl, ws=BAD, ws_bytes=need) == jl.JL_ERR_ALIGN
 
 
+def _paged(jl, q=GOOD, kp=GOOD, vp=GOOD, table=GOOD, lens=GOOD, out=GOOD, lse=GOOD, B=2, Hq=32, Hkv=8,
+           D=128, page_size=64, num_pages=10, max_pages=5, max_n=300, L=100, w=64, theta=1e6,
+           ws=GOOD, ws_bytes=1 << 24):
+    return jl.lib.jl_bifocal_decode_paged(q, kp, vp, table, lens, out, lse, B, Hq, Hkv, D, page_size,
+                                          num_pages, max_pages, max_n, L, w, theta, ws, ws_bytes, None)
+
+
+def test_decode_paged_argument_checks(jl):
+    """Rejected before any launch (no GPU needed)."""
+    for kw in ({"page_size": 32}, {"page_size": 96}, {"num_pages": 0}, {"max_pages": 0},
+               {"max_n": 321}, {"max_n": 0}, {"B": 0}, {"w": 0}, {"L": 0}, {"Hq": 3, "Hkv": 2}):
+        assert _paged(jl, **kw) == jl.JL_ERR_ARG, kw
+    for name in ("q", "kp", "vp", "table", "lens", "out", "lse"):
+        assert _paged(jl, **{name: None}) == jl.JL_ERR_ARG, name
+    assert _paged(jl, D=96) == jl.JL_ERR_UNSUPPORTED
+    assert _paged(jl, ws_bytes=16) == jl.JL_ERR_WORKSPACE
+    for name in ("q", "kp", "vp", "out", "lse"):
+        assert _paged(jl, **{name: BAD}) == jl.JL_ERR_ALIGN, name
+    assert _paged(jl, table=ctypes.c_void_p(0x1002)) == jl.JL_ERR_ALIGN
+    assert _paged(jl, lens=ctypes.c_void_p(0x1001)) == jl.JL_ERR_ALIGN
+
+
 def test_decode_workspace_size(jl):
     assert jl.jl_bifocal_decode_workspace_size(1, 32, 8, 0, 128) == 0
     assert jl.jl_bifocal_decode_workspace_size(1, 30, 8, 10, 128) == 0
@@ -133,6 +155,16 @@ def test_decode_workspace_size(jl):
     assert 0 < small <= big
     # partial o for every (head, split) at most: 256 splits
     assert big <= 256 + 1 * 32 * 256 * (128 + 2) * 4 + 512
+
+
+def test_decode_paged_workspace_size(jl):
+    """Sized for the longest sequence alone: at least the uniform plan's size,
+    the same for every max_n, 0 on bad sizes."""
+    assert jl.jl_bifocal_decode_paged_workspace_size(4, 32, 8, 0, 128) == 0
+    assert jl.jl_bifocal_decode_paged_workspace_size(4, 30, 8, 10, 128) == 0
+    sizes = {jl.jl_bifocal_decode_paged_workspace_size(4, 32, 8, n, 128) for n in (64, 8192, 131072)}
+    assert len(sizes) == 1
+    assert sizes.pop() >= jl.jl_bifocal_decode_workspace_size(4, 32, 8, 131072, 128)
 
 
 def test_rope_argument_checks(jl):

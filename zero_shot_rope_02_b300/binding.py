@@ -31,7 +31,8 @@ EXPORTS = (
     "jl_status_string", "jl_version", "jl_group_factor", "jl_rope_apply", "jl_bifocal_prefill",
     "jl_bifocal_decode_workspace_size", "jl_bifocal_decode", "jl_debug_grouped_positions",
     "jl_debug_tile_classes", "jl_debug_status", "jl_bifocal_decode_noalloc",
-    "jl_debug_wait_timeout", "jl_bifocal_prefill_chunk",
+    "jl_debug_wait_timeout", "jl_bifocal_prefill_chunk", "jl_bifocal_decode_paged",
+    "jl_bifocal_decode_paged_workspace_size",
 )
 
 
@@ -60,6 +61,9 @@ def _load() -> ctypes.CDLL:
                                     p, sz, p]),
         "jl_bifocal_decode_noalloc": (i32, [p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, i32,
                                             dbl, p]),
+        "jl_bifocal_decode_paged_workspace_size": (sz, [i32, i32, i32, i32, i32]),
+        "jl_bifocal_decode_paged": (i32, [p, p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, i32,
+                                          i32, i32, dbl, p, sz, p]),
         "jl_debug_grouped_positions": (i32, [i64, i64, p, p]),
         "jl_debug_tile_classes": (i32, [i32, i32, i32, p, p]),
         "jl_debug_status": (i32, [ctypes.POINTER(ctypes.c_int)]),
@@ -181,6 +185,10 @@ def jl_bifocal_prefill_chunk(q, k_cache, v_cache, n_past: int, L_pre: int, w: in
     return out, lse
 
 
+def jl_bifocal_decode_paged_workspace_size(B: int, Hq: int, Hkv: int, max_n: int, D: int) -> int:
+    return int(lib.jl_bifocal_decode_paged_workspace_size(B, Hq, Hkv, max_n, D))
+
+
 def jl_bifocal_decode_workspace_size(B: int, Hq: int, Hkv: int, n: int, D: int) -> int:
     return int(lib.jl_bifocal_decode_workspace_size(B, Hq, Hkv, n, D))
 
@@ -214,6 +222,42 @@ def jl_bifocal_decode(q, k_cache, v_cache, n: int, L_pre: int, w: int, theta: fl
                                  Hkv, int(n), n_cap, D, int(L_pre), int(w), float(theta),
                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
                                  _stream(stream)))
+    return out, lse
+
+
+def jl_bifocal_decode_paged(q, k_pages, v_pages, block_table, seq_lens, max_n: int, L_pre: int, w: int,
+                            theta: float, workspace=None, out=None, lse=None, stream=None):
+    """Bifocal decode of B sequences of their own lengths over a paged cache.
+    q [B,Hq,D]; pages [num_pages,page_size,Hkv,D] bf16 (exact RoPE);
+    block_table int32 [B,max_pages] and seq_lens int32 [B] on the device;
+    max_n >= every length.  ``workspace`` as for jl_bifocal_decode (sized for
+    max_n).  Returns (out bf16 [B,Hq,D], lse fp32 [B,Hq])."""
+    import torch
+
+    for t, nm in ((q, "q"), (k_pages, "k_pages"), (v_pages, "v_pages")):
+        _need(t, torch.bfloat16, nm)
+    _need(block_table, torch.int32, "block_table")
+    _need(seq_lens, torch.int32, "seq_lens")
+    B, Hq, D = q.shape
+    num_pages, page_size, Hkv, Dk = k_pages.shape
+    max_pages = block_table.shape[1]
+    if Dk != D or v_pages.shape != k_pages.shape or block_table.shape[0] != B or seq_lens.shape != (B,):
+        raise ValueError("pages [P, page_size, Hkv, D], block_table [B, max_pages], seq_lens [B]")
+    if workspace is None:
+        nbytes = jl_bifocal_decode_paged_workspace_size(B, Hq, Hkv, max_n, D)
+        workspace = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    _need(out, torch.bfloat16, "out")
+    _need(lse, torch.float32, "lse")
+    _check("jl_bifocal_decode_paged",
+           lib.jl_bifocal_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
+                                       _ptr(seq_lens), _ptr(out), _ptr(lse), B, Hq, Hkv, D, page_size,
+                                       num_pages, max_pages, int(max_n), int(L_pre), int(w), float(theta),
+                                       _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                       _stream(stream)))
     return out, lse
 
 

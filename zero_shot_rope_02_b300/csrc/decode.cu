@@ -55,6 +55,11 @@ struct DecodeArgs {
     int *status;
     int Hq, Hkv, n, w, g, splits, chunk;
     float scale_log2;        // tau * log2(e)
+    // paged variant: per-sequence lengths and the page table (device), the
+    // pages' row count, table width and the pretrained window (g per sequence)
+    const int *seq_lens;     // [B]
+    const int *block_table;  // [B, max_pages]
+    int page_size, max_pages, L;
 };
 
 // Named barrier over the compute warps only (the producer warp never joins).
@@ -80,7 +85,10 @@ struct DecCfg {
     static_assert(KPS3 * GRP * D * 4 <= 2 * kNS * BLOCK_BYTES, "reduction buffer");
 };
 
-template <int D, int GRP>
+// PAGED: the keys of sequence b live in pages of a shared pool, page p of it
+// at block_table[b][p]; its length n_b comes from seq_lens[b] and sets its own
+// g.  Otherwise the cache is [B, n_cap, Hkv, D] and every sequence has length n.
+template <int D, int GRP, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                   const DecodeArgs a, const __grid_constant__ jl::PhaseTable pt,
@@ -112,7 +120,18 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
-    const int n = a.n, g = a.g;
+    int n = a.n, g = a.g;
+    if constexpr (PAGED) {
+        // a length the plan or the page table cannot cover is clamped (never
+        // read past either) and reported
+        const int n_lim = min(a.max_pages * a.page_size, a.splits * a.chunk);
+        n = a.seq_lens[b];
+        if (n < 1 || n > n_lim) {
+            if (tid == 0 && split == 0 && hk == 0) jl::record_status(a.status, JL_ERR_GUARD);
+            n = min(max(n, 1), n_lim);
+        }
+        g = (n <= a.L) ? 1 : (n - 1) / a.L + 1;
+    }
     const int j_begin = split * a.chunk;
     const int j_end = min(n, j_begin + a.chunk);
     const int nblk = (j_end - j_begin + kKB - 1) / kKB;
@@ -140,8 +159,14 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (!(ok = wait_bar(empty(s), ((blk / kNS) & 1) ^ 1, wc))) break;
                 mbar_arrive_expect_tx(full(s), 2 * C::BLOCK_BYTES);
                 const int row = j_begin + blk * kKB;
-                tma_load_4d(sbase + C::OFF_K + s * C::BLOCK_BYTES, &tk, full(s), 0, hk, row, b);
-                tma_load_4d(sbase + C::OFF_V + s * C::BLOCK_BYTES, &tv, full(s), 0, hk, row, b);
+                int r_in = row, unit = b;
+                if constexpr (PAGED) {
+                    // a page id outside the pool reads zeros (TMA bounds), never faults
+                    unit = a.block_table[(size_t)b * a.max_pages + row / a.page_size];
+                    r_in = row % a.page_size;
+                }
+                tma_load_4d(sbase + C::OFF_K + s * C::BLOCK_BYTES, &tk, full(s), 0, hk, r_in, unit);
+                tma_load_4d(sbase + C::OFF_V + s * C::BLOCK_BYTES, &tv, full(s), 0, hk, r_in, unit);
                 issued = blk + 1;
             }
             if (!ok)
@@ -195,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // rotation chain of this thread's next remote key
     jl::f32x2 zc[4], zs[4];
     int chain_next = -1;  // key the chain currently refers to
-    const bool uni = rot.uni != 0;
+    const bool uni = PAGED ? (KPS % g == 0) : (rot.uni != 0);
     auto anchor = [&](int j) {
         const int dj = jl::delta_pos(j, g);
 #pragma unroll
@@ -211,9 +236,20 @@ __global__ void __launch_bounds__(kThreads, 2)
     jl::f32x2 rcs[4], rsn[4], rns[4];
 #pragma unroll
     for (int q = 0; q < 4; q++) {
-        rcs[q] = *reinterpret_cast<const jl::f32x2 *>(rot.c + 8 * c + 2 * q);
-        rsn[q] = *reinterpret_cast<const jl::f32x2 *>(rot.s + 8 * c + 2 * q);
-        rns[q] = *reinterpret_cast<const jl::f32x2 *>(rot.ns + 8 * c + 2 * q);
+        if constexpr (PAGED) {
+            // this sequence's g: delta moves by KPS/g - KPS per KPS keys (g | KPS)
+            const int step = KPS / g - KPS;
+            float s0, c0, s1, c1;
+            jl::phase_sincos(step, pt.f[8 * c + 2 * q], &s0, &c0);
+            jl::phase_sincos(step, pt.f[8 * c + 2 * q + 1], &s1, &c1);
+            rcs[q] = jl::f2(c0, c1);
+            rsn[q] = jl::f2(s0, s1);
+            rns[q] = jl::f2(-s0, -s1);
+        } else {
+            rcs[q] = *reinterpret_cast<const jl::f32x2 *>(rot.c + 8 * c + 2 * q);
+            rsn[q] = *reinterpret_cast<const jl::f32x2 *>(rot.s + 8 * c + 2 * q);
+            rns[q] = *reinterpret_cast<const jl::f32x2 *>(rot.ns + 8 * c + 2 * q);
+        }
     }
     jl::f32x2 acc[GRP][4];
 #pragma unroll
@@ -330,7 +366,10 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll 2
         for (int it = 0; it < VITEMS; it++) {
             const int kk = r3 + KPS3 * it;
-            const uint4 v4 = *reinterpret_cast<const uint4 *>(vblk + kk * (D * 2) + 16 * dc);
+            uint4 v4 = *reinterpret_cast<const uint4 *>(vblk + kk * (D * 2) + 16 * dc);
+            // a page's rows past the sequence hold whatever the pool held: zero
+            // them (their p is 0, but 0 * NaN would still poison O)
+            if (PAGED && j0 + kk >= j_end) v4 = make_uint4(0u, 0u, 0u, 0u);
             const jl::f32x2 vx[4] = {jl::bf16x2_to_f2(v4.x), jl::bf16x2_to_f2(v4.y), jl::bf16x2_to_f2(v4.z),
                                      jl::bf16x2_to_f2(v4.w)};
 #pragma unroll
@@ -454,6 +493,19 @@ Plan make_plan(int B, int Hkv, int n)
     return Plan{(int)splits, (int)chunk, (int)per_head};
 }
 
+// Paged batches mix lengths, so the split count is sized for the longest
+// sequence as if it alone filled the GPU (two CTAs per SM over its kv heads);
+// the splits of shorter sequences past their end exit at once.
+Plan make_paged_plan(int Hkv, int max_n)
+{
+    long long per_head = (148LL * 2 + Hkv - 1) / Hkv;
+    if (per_head > 256) per_head = 256;
+    long long chunk = (max_n + per_head - 1) / per_head;
+    chunk = (chunk + kKB - 1) / kKB * kKB;
+    long long splits = (max_n + chunk - 1) / chunk;
+    return Plan{(int)splits, (int)chunk, (int)per_head};
+}
+
 size_t ws_layout(int B, int Hq, int Hkv, int D, const Plan &p, size_t *off_ml, size_t *off_o)
 {
     size_t cnt = ((size_t)B * Hkv * sizeof(int) + 255) / 256 * 256;
@@ -499,12 +551,12 @@ bool host_tables(int D, double theta, int g, const jl::PhaseTable **pt, const De
     return true;
 }
 
-template <int D, int GRP>
-int launch(const DecodeArgs &a, int B, int n_cap, const void *k_cache, const void *v_cache,
+template <int D, int GRP, bool PAGED>
+int launch(const DecodeArgs &a, int B, const CUtensorMap &tk, const CUtensorMap &tv,
            const jl::PhaseTable &pt, const DecRot &rot, cudaStream_t st)
 {
     using C = DecCfg<D, GRP>;
-    auto kern = decode_kernel<D, GRP>;
+    auto kern = decode_kernel<D, GRP, PAGED>;
     static bool attr_set[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return jl::cuda_status(cudaGetLastError());
@@ -513,53 +565,49 @@ int launch(const DecodeArgs &a, int B, int n_cap, const void *k_cache, const voi
         if (e != cudaSuccess) return jl::cuda_status(e);
         attr_set[dev] = true;
     }
-    CUtensorMap tk, tv;
-    // only rows [0, n) are mapped: the block that holds key n-1 reads zeros past
-    // it, never the cache's unused capacity (0 * NaN would poison P.V)
-    if (!jl::make_bshd_map(&tk, k_cache, B, a.n, n_cap, a.Hkv, D, D, kKB, false) ||
-        !jl::make_bshd_map(&tv, v_cache, B, a.n, n_cap, a.Hkv, D, D, kKB, false))
-        return JL_ERR_CUDA;
     dim3 grid(a.splits, a.Hkv, B);
     kern<<<grid, kThreads, C::SMEM, st>>>(tk, tv, a, pt, rot);
     return jl::cuda_status(cudaGetLastError());
 }
 
-}  // namespace
-
-extern "C" size_t jl_bifocal_decode_workspace_size(int B, int Hq, int Hkv, int n, int D)
+template <bool PAGED>
+int dispatch(int D, int grp, const DecodeArgs &a, int B, const CUtensorMap &tk, const CUtensorMap &tv,
+             const jl::PhaseTable &pt, const DecRot &rot, cudaStream_t st)
 {
-    if (!shapes_ok(B, Hq, Hkv, n, D)) return 0;
-    Plan p = make_plan(B, Hkv, n);
-    return ws_layout(B, Hq, Hkv, D, p, nullptr, nullptr);
+    if (D == 128) {
+        switch (grp) {
+        case 1: return launch<128, 1, PAGED>(a, B, tk, tv, pt, rot, st);
+        case 2: return launch<128, 2, PAGED>(a, B, tk, tv, pt, rot, st);
+        case 4: return launch<128, 4, PAGED>(a, B, tk, tv, pt, rot, st);
+        default: return launch<128, 8, PAGED>(a, B, tk, tv, pt, rot, st);
+        }
+    }
+    switch (grp) {
+    case 1: return launch<64, 1, PAGED>(a, B, tk, tv, pt, rot, st);
+    case 2: return launch<64, 2, PAGED>(a, B, tk, tv, pt, rot, st);
+    case 4: return launch<64, 4, PAGED>(a, B, tk, tv, pt, rot, st);
+    default: return launch<64, 8, PAGED>(a, B, tk, tv, pt, rot, st);
+    }
 }
 
-extern "C" int jl_bifocal_decode(const void *q, const void *k_cache, const void *v_cache, void *out,
-                                 float *lse, int B, int Hq, int Hkv, int n, int n_cap, int D,
-                                 int L_pre, int w, double theta, void *workspace, size_t ws_bytes,
-                                 void *stream)
+// The argument checks and workspace layout both entry points share; fills the
+// length-independent fields of `a`.
+int common_setup(DecodeArgs &a, const void *q, void *out, float *lse, int B, int Hq, int Hkv, int n,
+                 int D, int L_pre, int w, double theta, void *workspace, size_t ws_bytes, bool paged)
 {
-    if (!q || !k_cache || !v_cache || !out || !lse) return JL_ERR_ARG;
-    if (B < 1 || Hq < 1 || Hkv < 1 || n < 1 || n_cap < n || L_pre < 1 || w < 1 ||
-        !(theta > 0.0) || Hq % Hkv != 0)
+    if (!q || !out || !lse) return JL_ERR_ARG;
+    if (B < 1 || Hq < 1 || Hkv < 1 || n < 1 || L_pre < 1 || w < 1 || !(theta > 0.0) || Hq % Hkv != 0)
         return JL_ERR_ARG;
     if (D != 64 && D != 128) return JL_ERR_UNSUPPORTED;
     const int grp = Hq / Hkv;
     if (grp != 1 && grp != 2 && grp != 4 && grp != 8) return JL_ERR_UNSUPPORTED;
-    if (!jl::aligned16(q) || !jl::aligned16(k_cache) || !jl::aligned16(v_cache) ||
-        !jl::aligned16(out) || !jl::aligned16(lse))
-        return JL_ERR_ALIGN;
-    if ((long long)B * n_cap * Hkv * D > ((long long)1 << 46)) return JL_ERR_OVERFLOW;
-    Plan p = make_plan(B, Hkv, n);
+    if (!jl::aligned16(q) || !jl::aligned16(out) || !jl::aligned16(lse)) return JL_ERR_ALIGN;
+    Plan p = paged ? make_paged_plan(Hkv, n) : make_plan(B, Hkv, n);
     size_t off_ml = 0, off_o = 0;
     size_t need = ws_layout(B, Hq, Hkv, D, p, &off_ml, &off_o);
     if (!workspace || ws_bytes < need) return JL_ERR_WORKSPACE;
     if (!jl::aligned16(workspace)) return JL_ERR_ALIGN;
-    const int g = (int)jl::group_factor_host(n, L_pre);
-    const jl::PhaseTable *pt = nullptr;
-    const DecRot *rot = nullptr;
-    if (!host_tables(D, theta, g, &pt, &rot)) return JL_ERR_ARG;
-
-    DecodeArgs a;
+    memset(&a, 0, sizeof(a));
     a.q = (const __nv_bfloat16 *)q;
     a.out = (__nv_bfloat16 *)out;
     a.lse = lse;
@@ -572,25 +620,83 @@ extern "C" int jl_bifocal_decode(const void *q, const void *k_cache, const void 
     a.Hkv = Hkv;
     a.n = n;
     a.w = w;
-    a.g = g;
+    a.L = L_pre;
     a.splits = p.splits;
     a.chunk = p.chunk;
     a.scale_log2 = (float)(1.0 / sqrt((double)D) * 1.4426950408889634);
-    cudaStream_t st = (cudaStream_t)stream;
-    if (D == 128) {
-        switch (grp) {
-        case 1: return launch<128, 1>(a, B, n_cap, k_cache, v_cache, *pt, *rot, st);
-        case 2: return launch<128, 2>(a, B, n_cap, k_cache, v_cache, *pt, *rot, st);
-        case 4: return launch<128, 4>(a, B, n_cap, k_cache, v_cache, *pt, *rot, st);
-        default: return launch<128, 8>(a, B, n_cap, k_cache, v_cache, *pt, *rot, st);
-        }
-    }
-    switch (grp) {
-    case 1: return launch<64, 1>(a, B, n_cap, k_cache, v_cache, *pt, *rot, st);
-    case 2: return launch<64, 2>(a, B, n_cap, k_cache, v_cache, *pt, *rot, st);
-    case 4: return launch<64, 4>(a, B, n_cap, k_cache, v_cache, *pt, *rot, st);
-    default: return launch<64, 8>(a, B, n_cap, k_cache, v_cache, *pt, *rot, st);
-    }
+    return JL_OK;
+}
+
+}  // namespace
+
+extern "C" size_t jl_bifocal_decode_workspace_size(int B, int Hq, int Hkv, int n, int D)
+{
+    if (!shapes_ok(B, Hq, Hkv, n, D)) return 0;
+    Plan p = make_plan(B, Hkv, n);
+    return ws_layout(B, Hq, Hkv, D, p, nullptr, nullptr);
+}
+
+extern "C" size_t jl_bifocal_decode_paged_workspace_size(int B, int Hq, int Hkv, int max_n, int D)
+{
+    if (!shapes_ok(B, Hq, Hkv, max_n, D)) return 0;
+    return ws_layout(B, Hq, Hkv, D, make_paged_plan(Hkv, max_n), nullptr, nullptr);
+}
+
+extern "C" int jl_bifocal_decode(const void *q, const void *k_cache, const void *v_cache, void *out,
+                                 float *lse, int B, int Hq, int Hkv, int n, int n_cap, int D,
+                                 int L_pre, int w, double theta, void *workspace, size_t ws_bytes,
+                                 void *stream)
+{
+    if (!k_cache || !v_cache) return JL_ERR_ARG;
+    if (n_cap < n) return JL_ERR_ARG;
+    DecodeArgs a;
+    int rc = common_setup(a, q, out, lse, B, Hq, Hkv, n, D, L_pre, w, theta, workspace, ws_bytes, false);
+    if (rc != JL_OK) return rc;
+    if (!jl::aligned16(k_cache) || !jl::aligned16(v_cache)) return JL_ERR_ALIGN;
+    if ((long long)B * n_cap * Hkv * D > ((long long)1 << 46)) return JL_ERR_OVERFLOW;
+    a.g = (int)jl::group_factor_host(n, L_pre);
+    const jl::PhaseTable *pt = nullptr;
+    const DecRot *rot = nullptr;
+    if (!host_tables(D, theta, a.g, &pt, &rot)) return JL_ERR_ARG;
+    CUtensorMap tk, tv;
+    // only rows [0, n) are mapped: the block that holds key n-1 reads zeros past
+    // it, never the cache's unused capacity (0 * NaN would poison P.V)
+    if (!jl::make_bshd_map(&tk, k_cache, B, n, n_cap, Hkv, D, D, kKB, false) ||
+        !jl::make_bshd_map(&tv, v_cache, B, n, n_cap, Hkv, D, D, kKB, false))
+        return JL_ERR_CUDA;
+    return dispatch<false>(D, Hq / Hkv, a, B, tk, tv, *pt, *rot, (cudaStream_t)stream);
+}
+
+extern "C" int jl_bifocal_decode_paged(const void *q, const void *k_pages, const void *v_pages,
+                                       const int *block_table, const int *seq_lens, void *out,
+                                       float *lse, int B, int Hq, int Hkv, int D, int page_size,
+                                       int num_pages, int max_pages, int max_n, int L_pre, int w,
+                                       double theta, void *workspace, size_t ws_bytes, void *stream)
+{
+    if (!k_pages || !v_pages || !block_table || !seq_lens) return JL_ERR_ARG;
+    if (page_size < kKB || page_size % kKB != 0 || num_pages < 1 || max_pages < 1 ||
+        (long long)max_pages * page_size > 0x7fffffffLL || max_n > max_pages * page_size)
+        return JL_ERR_ARG;
+    DecodeArgs a;
+    int rc = common_setup(a, q, out, lse, B, Hq, Hkv, max_n, D, L_pre, w, theta, workspace, ws_bytes, true);
+    if (rc != JL_OK) return rc;
+    if (!jl::aligned16(k_pages) || !jl::aligned16(v_pages) ||
+        (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+        return JL_ERR_ALIGN;
+    if ((long long)num_pages * page_size * Hkv * D > ((long long)1 << 46)) return JL_ERR_OVERFLOW;
+    a.seq_lens = seq_lens;
+    a.block_table = block_table;
+    a.page_size = page_size;
+    a.max_pages = max_pages;
+    const jl::PhaseTable *pt = nullptr;
+    const DecRot *rot = nullptr;
+    if (!host_tables(D, theta, 1, &pt, &rot)) return JL_ERR_ARG;  // per-sequence g on the device
+    CUtensorMap tk, tv;
+    // the pool as num_pages units of page_size rows: a page id outside it reads zeros
+    if (!jl::make_bshd_map(&tk, k_pages, num_pages, page_size, page_size, Hkv, D, D, kKB, false) ||
+        !jl::make_bshd_map(&tv, v_pages, num_pages, page_size, page_size, Hkv, D, D, kKB, false))
+        return JL_ERR_CUDA;
+    return dispatch<true>(D, Hq / Hkv, a, B, tk, tv, *pt, *rot, (cudaStream_t)stream);
 }
 
 // ---------------------------------------------------------------- no-allocation entry point
