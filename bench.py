@@ -215,6 +215,13 @@ def run_ours(args, rank, world, dev):
                           stream, dev, reps=max(3, args.steps))
     chunk_flops = chunk_prefill_flops(B, Hq, D, S_new, n_past)
     paged = paged_decode(jl, dev, stream, peaks, args)
+    # RoPE fused into the cache write: the whole context's raw k and v into a cache
+    kc_dst = torch.empty_like(k)
+    vc_dst = torch.empty_like(v)
+    cw_ms = time_calls(lambda: jl.jl_rope_cache_write(k, v, kc_dst, vc_dst, 0, theta, stream=stream),
+                       stream, dev, reps=max(3, args.steps))
+    cw_bytes = 4 * k.numel() * k.element_size()  # read k and v, write both
+    del kc_dst, vc_dst
     if jl.jl_debug_status() != 0:
         raise RuntimeError("device status word set by the chunk run")
 
@@ -233,6 +240,9 @@ def run_ours(args, rank, world, dev):
                        "bifocal_overhead": round(avg_prefill_ms / plain_ms - 1.0, 4)},
         "decode": decode,
         "paged_decode": paged,
+        "rope_cache_write": {"rows": S, "us": round(1e3 * cw_ms, 2),
+                             "gbs": round(cw_bytes / (cw_ms * 1e-3) / 1e9, 1),
+                             "frac_of_hbm": round(cw_bytes / (cw_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)},
         "chunk": {"S_new": S_new, "n_past": n_past, "ms": round(chunk_ms, 3),
                   "tflops": round(chunk_flops / (chunk_ms * 1e-3) / 1e12, 2),
                   "frac_of_bf16_peak": round(chunk_flops / (chunk_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)},

@@ -110,6 +110,22 @@ int jl_rope_apply(void *x, int B, int S, int H, int D, int64_t pos0, double thet
                   void *stream);
 
 /*
+ * Exact RoPE fused into the KV-cache write (the step before the attention
+ * path): the S_new new tokens' raw keys and their values go to cache rows
+ * n_past .. n_past+S_new-1, each key rotated at its position on the way --
+ * one read and one write of each byte.  The rotated keys are bit-identical to
+ * jl_rope_apply at pos0 = n_past.
+ *   k_raw, v   device bf16 [B, S_new, H, D]; k_raw before RoPE
+ *   k_cache, v_cache  device bf16 [B, n_cap, H, D]; only rows
+ *              n_past..n_past+S_new-1 are written
+ *   D a multiple of 16 (<= 256), n_past >= 0, n_past + S_new <= n_cap
+ * Returns JL_OK, JL_ERR_ARG, JL_ERR_ALIGN, JL_ERR_UNSUPPORTED,
+ * JL_ERR_OVERFLOW or JL_ERR_CUDA.
+ */
+int jl_rope_cache_write(const void *k_raw, const void *v, void *k_cache, void *v_cache, int B,
+                        int S_new, int H, int D, int n_past, int n_cap, double theta, void *stream);
+
+/*
  * Bifocal causal GQA prefill attention (one TMA + tcgen05 kernel).
  * The three attention passes of the pages -- local(window, exact RoPE),
  * remote(all, aliased) and remote(window, aliased), merged by

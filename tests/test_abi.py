@@ -178,6 +178,22 @@ def test_rope_argument_checks(jl):
     assert f(GOOD, 1, 4, 2, 8, (1 << 62) - 2, 1e4, None) == jl.JL_ERR_OVERFLOW
 
 
+def _cache_write(jl, k=GOOD, v=GOOD, kc=GOOD, vc=GOOD, B=1, S_new=16, H=8, D=128, n_past=10, n_cap=26,
+                 theta=1e6):
+    return jl.lib.jl_rope_cache_write(k, v, kc, vc, B, S_new, H, D, n_past, n_cap, theta, None)
+
+
+def test_rope_cache_write_argument_checks(jl):
+    """Rejected before any launch (no GPU needed)."""
+    for kw in ({"B": 0}, {"S_new": 0}, {"H": 0}, {"n_past": -1}, {"n_cap": 25}, {"theta": 0.0},
+               {"k": None}, {"vc": None}):
+        assert _cache_write(jl, **kw) == jl.JL_ERR_ARG, kw
+    for D in (8, 24, 100, 272):
+        assert _cache_write(jl, D=D) == jl.JL_ERR_UNSUPPORTED, D
+    for name in ("k", "v", "kc", "vc"):
+        assert _cache_write(jl, **{name: BAD}) == jl.JL_ERR_ALIGN, name
+
+
 def test_debug_argument_checks(jl):
     assert jl.lib.jl_debug_grouped_positions(0, 4, GOOD, None) == jl.JL_ERR_ARG
     assert jl.lib.jl_debug_grouped_positions(4, 4, None, None) == jl.JL_ERR_ARG

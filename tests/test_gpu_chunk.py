@@ -1,5 +1,6 @@
-"""Prefill of a chunk over an existing cache (jl_bifocal_prefill_chunk) and the
-capacity guard of every cache-reading call, against the fp64 oracle.
+"""Prefill of a chunk over an existing cache (jl_bifocal_prefill_chunk), the
+capacity guard of every cache-reading call, and the RoPE-fused cache write
+that fills the cache (jl_rope_cache_write), against the fp64 oracle.
 
 A chunk is S_new queries at positions n_past..n_past+S_new-1 over the keys at
 0..n_past+S_new-1, with s = n_past + S_new setting g: the rows a full prefill
@@ -112,3 +113,28 @@ def test_chunk_benchmark_shape_sampled(jl, orc, dev):
     ref_o, ref_l = orc.bifocal_rows(q_rows, k_f, v_f, n_past + rows, s, L, w, 1e6)
     helpers.compare(helpers.bf16_to_f64(out[:, rows]), lse[:, :, rows].cpu().numpy(), ref_o, ref_l,
                     "chunk 8K over 120K (sampled rows)")
+
+
+@pytest.mark.parametrize("B,S_new,H,D,n_past,n_cap", [(2, 300, 8, 128, 777, 1200), (1, 65, 4, 64, 0, 65)])
+def test_rope_cache_write(jl, orc, dev, B, S_new, H, D, n_past, n_cap):
+    """RoPE fused into the cache write: the written keys are jl_rope_apply's
+    bits, the values are copied, no other cache row is touched, and the keys
+    match the oracle's RoPE within one bf16 rounding."""
+    import torch
+
+    theta = 1e6
+    k_t, k_f = helpers.bf16_pair((B, S_new, H, D), 14, 1)
+    v_t, _ = helpers.bf16_pair((B, S_new, H, D), 14, 2)
+    k, v = k_t.to(dev), v_t.to(dev)
+    kc = torch.full((B, n_cap, H, D), float("nan"), dtype=torch.bfloat16, device=dev)
+    vc = torch.full_like(kc, float("nan"))
+    jl.jl_rope_cache_write(k, v, kc, vc, n_past, theta)
+    rows = slice(n_past, n_past + S_new)
+    assert torch.equal(kc[:, rows], jl.jl_rope_apply(k.clone(), n_past, theta))
+    assert torch.equal(vc[:, rows], v)
+    for c in (kc, vc):
+        assert torch.isnan(c[:, :n_past].float()).all() and torch.isnan(c[:, n_past + S_new:].float()).all()
+    got = helpers.bf16_to_f64(kc[:, rows])
+    ref = orc.rope(k_f, n_past, theta)
+    # one rounding to bf16 of an fp32 result: within 2^-8 relative (+ fp32 slack)
+    assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-5 * np.abs(k_f).max())

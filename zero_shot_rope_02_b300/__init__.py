@@ -11,7 +11,7 @@ _BINDING_NAMES = (
     "jl_bifocal_prefill", "jl_debug_grouped_positions", "jl_debug_status", "jl_debug_tile_classes",
     "jl_group_factor", "jl_rope_apply", "jl_version", "lib", "status_string",
     "jl_bifocal_decode_noalloc", "jl_debug_wait_timeout", "jl_bifocal_prefill_chunk",
-    "jl_bifocal_decode_paged", "jl_bifocal_decode_paged_workspace_size",
+    "jl_bifocal_decode_paged", "jl_bifocal_decode_paged_workspace_size", "jl_rope_cache_write",
 )
 
 __all__ = list(_BINDING_NAMES)

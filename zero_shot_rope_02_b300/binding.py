@@ -32,7 +32,7 @@ EXPORTS = (
     "jl_bifocal_decode_workspace_size", "jl_bifocal_decode", "jl_debug_grouped_positions",
     "jl_debug_tile_classes", "jl_debug_status", "jl_bifocal_decode_noalloc",
     "jl_debug_wait_timeout", "jl_bifocal_prefill_chunk", "jl_bifocal_decode_paged",
-    "jl_bifocal_decode_paged_workspace_size",
+    "jl_bifocal_decode_paged_workspace_size", "jl_rope_cache_write",
 )
 
 
@@ -53,6 +53,7 @@ def _load() -> ctypes.CDLL:
         "jl_version": (ctypes.c_char_p, []),
         "jl_group_factor": (i32, [i64, i64, ctypes.POINTER(ctypes.c_int32)]),
         "jl_rope_apply": (i32, [p, i32, i32, i32, i32, i64, dbl, p]),
+        "jl_rope_cache_write": (i32, [p, p, p, p, i32, i32, i32, i32, i32, i32, dbl, p]),
         "jl_bifocal_prefill": (i32, [p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, dbl, p]),
         "jl_bifocal_prefill_chunk": (i32, [p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                            dbl, p]),
@@ -132,6 +133,24 @@ def jl_rope_apply(x, pos0: int, theta: float, stream=None):
     _check("jl_rope_apply", lib.jl_rope_apply(_ptr(x), B, S, H, D, int(pos0), float(theta),
                                               _stream(stream)))
     return x
+
+
+def jl_rope_cache_write(k_raw, v, k_cache, v_cache, n_past: int, theta: float, stream=None):
+    """RoPE fused into the cache write: k_raw / v [B,S_new,H,D] (k before RoPE)
+    into cache rows n_past.. of k_cache / v_cache [B,n_cap,H,D], k rotated."""
+    import torch
+
+    for t, nm in ((k_raw, "k_raw"), (v, "v"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, nm)
+    B, S_new, H, D = k_raw.shape
+    n_cap = k_cache.shape[1]
+    if v.shape != k_raw.shape or v_cache.shape != k_cache.shape or k_cache.shape[0] != B or \
+            k_cache.shape[2:] != (H, D):
+        raise ValueError("k_raw / v [B,S_new,H,D] and caches [B,n_cap,H,D]")
+    _check("jl_rope_cache_write",
+           lib.jl_rope_cache_write(_ptr(k_raw), _ptr(v), _ptr(k_cache), _ptr(v_cache), B, S_new, H, D,
+                                   int(n_past), n_cap, float(theta), _stream(stream)))
+    return k_cache, v_cache
 
 
 def jl_bifocal_prefill(q, k, v, L_pre: int, w: int, theta: float, out=None, lse=None,
