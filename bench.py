@@ -38,7 +38,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one 128K bifocal prefill launch from the ncu
 # launch list in profiles/launches_bench_prefill128k_decode128k.md, valid only
 # for the prefill source it was measured on (first 16 hex digits of its sha256).
-PREFILL_TRAFFIC = {"sha256_16": "d5731ef90cb78d36", "bytes": 3.568e9 + 1.058e9}
+PREFILL_TRAFFIC = {"sha256_16": "42ec6803786d95ff", "bytes": 3.554e9 + 1.058e9}
 
 
 def prefill_traffic():

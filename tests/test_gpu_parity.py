@@ -227,3 +227,28 @@ def test_prefill_benchmark_configs_sampled(jl, orc, dev, name, B, Hq, Hkv, S, L,
     g = orc.group_factor(S, L)
     rows = helpers.sample_rows(S, L, w, g, n_random=24, seed=seed)
     _prefill_case(jl, orc, dev, B, Hq, Hkv, S, 128, L, w, 1e6, seed=seed, rows=rows)
+
+
+def test_prefill_scores_jumping_by_thousands(jl, orc, dev):
+    """Later keys (x 2^6) and all queries (x 2^3) scaled so that a row's maximum
+    jumps by hundreds to thousands of log2 units between tiles: the running
+    offset must follow without P overflowing (exact power-of-two rescales).
+    Run with L >= S (every tile exact, bf16 operands): at scores this large
+    the fp16 rounding of corrected operands alone would move a score by about
+    one unit, which is outside that path's stated operand range."""
+    import torch
+
+    B, Hq, Hkv, S, D, L, w = 1, 2, 1, 700, 128, 1000, 150
+    q_t, q_f = helpers.bf16_pair((B, S, Hq, D), 15, 0, scale=8.0)
+    k_t, k_f = helpers.bf16_pair((B, S, Hkv, D), 15, 1)
+    # v x 2^-2: one key takes nearly all the weight here, so the bf16 rounding
+    # of P and of out lands on |out| undivided; small v keeps that inside 1e-2
+    v_t, v_f = helpers.bf16_pair((B, S, Hkv, D), 15, 2, scale=0.25)
+    k_t[:, 300:] *= 64.0
+    k_f[:, 300:] *= 64.0
+    out, lse = jl.jl_bifocal_prefill(_cuda(q_t, dev), _cuda(k_t, dev), _cuda(v_t, dev), L, w, 1e6)
+    assert jl.jl_debug_status() == 0
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    ref_o, ref_l = orc.bifocal_prefill(q_f, k_f, v_f, L, w, 1e6)
+    assert float(np.max(ref_l)) > 500.0  # the jump is really there
+    helpers.compare(helpers.bf16_to_f64(out), lse.cpu().numpy(), ref_o, ref_l, "scores jumping")

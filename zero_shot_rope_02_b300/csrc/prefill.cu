@@ -629,9 +629,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (m_cur == -INFINITY) {
                             m_cur = cm;  // the first half of this row holds only zeros
                         } else {
-                            const float k = fminf(ceilf(cm - m_cur), 200.f);
+                            // an integer step to at least the new maximum, so the
+                            // factor is an exact power of two (0 once below the
+                            // smallest fp32 subnormal) and no P exceeds 2^8
+                            const float k = ceilf(cm - m_cur);
                             m_cur += k;
-                            f = ldexpf(1.f, -(int)k);  // exact power of two
+                            f = k >= 150.f ? 0.f : ldexpf(1.f, -(int)k);
                         }
                     }
                     if (hh > 0 && __any_sync(0xffffffffu, raise && f != 1.f)) {
