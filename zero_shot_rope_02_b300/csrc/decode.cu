@@ -19,6 +19,13 @@
 // the same amount every KPS keys, so each key's rotation is the previous one
 // times a constant; the chain is re-anchored from the exact fixed-point
 // phase every kReanchorBlocks blocks.  Other g take the exact phase per key.
+//
+// The paged variant serves a batch whose sequences have their own lengths:
+// each CTA reads its sequence's length from the device and derives from it
+// g, the exact / remote split and the chain's step rotation, and the
+// producer finds each 64-key block's page in the sequence's block table.  Its
+// split plan is sized for the longest sequence; splits past a shorter
+// sequence's end load nothing and leave an empty partial for the merge.
 #include <math.h>
 #include <string.h>
 
