@@ -250,7 +250,13 @@ def run_ours(args, rank, world, dev):
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
                      "traffic": prefill_traffic(), "kernel": "prefill_kernel<128,2>",
-                     "peak_source": f"{peaks_src} bf16 burst"},
+                     "peak_source": f"{peaks_src} bf16 burst",
+                     # also reported: the back-to-back cuBLAS figure, taken at the
+                     # power-capped clock that loop settles to (this kernel runs
+                     # at higher clocks, so `frac` against the burst peak is the
+                     # conservative headline)
+                     "sustained_peak": peaks["bf16_tflops_sustained"],
+                     "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4)},
         "gpu_launches": 2 * args.steps,
         "clocks": clk.summary(),
     }
