@@ -62,6 +62,10 @@ class Oracle:
             fn = getattr(lib, name)
             fn.restype = ctypes.c_int
             fn.argtypes = sig
+        lib.oracle_bifocal_rows_ex.restype = ctypes.c_int
+        lib.oracle_bifocal_rows_ex.argtypes = sig[:14] + [i64] + sig[14:]
+        lib.oracle_group_factor_shift.restype = i64
+        lib.oracle_group_factor_shift.argtypes = [i64, i64, i64]
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_num_threads.argtypes = []
         self.lib = lib
@@ -111,6 +115,33 @@ class Oracle:
         """Three passes merged by inclusion-exclusion; same contract as bifocal_rows."""
         return self._attn("oracle_bifocal_rows_3pass", q, k, v, qpos, s_len, L, w, theta)
 
+    def group_factor_shift(self, s: int, L: int, w: int) -> int:
+        """Smallest g with floor((s-1)/g) + w - floor(w/g) <= L-1 (query-shift
+        variant; literal search), -1 if none."""
+        return int(self.lib.oracle_group_factor_shift(int(s), int(L), int(w)))
+
+    def bifocal_rows_ex(self, q, k, v, qpos, s_len, L, w, theta, flags):
+        """bifocal_rows with variant flags (PER_QUERY_G | SLIDING | QUERY_SHIFT)."""
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        B, Sq, Hq, D = q.shape
+        Bk, Sk, Hkv, Dk = k.shape
+        assert Bk == B and Dk == D and v.shape == k.shape
+        qpos = np.ascontiguousarray(np.asarray(qpos, dtype=np.int64))
+        assert qpos.shape == (Sq,)
+        out = np.empty((B, Sq, Hq, D), dtype=np.float64)
+        lse = np.empty((B, Hq, Sq), dtype=np.float64)
+        rc = self.lib.oracle_bifocal_rows_ex(_ptr(q), _ptr(k), _ptr(v), B, Sq, Hq, Hkv, Sk, D, _ptr(qpos),
+                                             int(s_len), int(L), int(w), float(theta), int(flags),
+                                             _ptr(out), _ptr(lse))
+        if rc != 0:
+            raise ValueError("oracle_bifocal_rows_ex: invalid arguments")
+        return out, lse
+
+    def bifocal_prefill_ex(self, q, k, v, L, w, theta, flags):
+        """Full causal prefill with variant flags."""
+        S = q.shape[1]
+        return self.bifocal_rows_ex(q, k, v, np.arange(S), S, L, w, theta, flags)
+
     def bifocal_prefill(self, q, k, v, L, w, theta):
         """Full causal prefill: every row of q [B,S,Hq,D], s = S."""
         S = q.shape[1]
@@ -121,6 +152,11 @@ class Oracle:
         n = k_cache.shape[1]
         return self.bifocal_rows(q, k_cache, v_cache, np.array([n - 1]), n, L, w, theta)
 
+
+# Variant flags of bifocal_rows_ex (values shared with oracle.c's ORACLE_* macros).
+PER_QUERY_G = 1
+SLIDING = 2
+QUERY_SHIFT = 4
 
 _default = None
 

@@ -73,3 +73,63 @@ def bifocal_from_raw(qr, kr, vr, L: int, w: int, theta: float):
         out[:, h, :] = (p @ vr[:, hk, :]) / Z[:, None]
         lse[h] = m[:, 0] + np.log(Z)
     return out, lse, qx, kx
+
+
+# ---------------------------------------------------------------- variants
+PER_QUERY_G, SLIDING, QUERY_SHIFT = 1, 2, 4
+
+
+def smallest_group_shift(s: int, L: int, w: int):
+    """Smallest g >= 1 such that, with the query's aliased position shifted by
+    w - floor(w/g), every aliased distance floor(i/g) + shift - floor(j/g),
+    0 <= j <= i < s, stays below L; None if no g up to max(s, w) + 1 does.
+    Checked pair by pair."""
+    for g in range(1, max(s, w) + 2):
+        shift = w - w // g
+        if max(i // g + shift - j // g for i in range(s) for j in range(i + 1)) <= L - 1:
+            return g
+    return None
+
+
+def bifocal_variant_from_raw(qr, kr, vr, L: int, w: int, theta: float, flags: int):
+    """Variants of bifocal_from_raw, from raw vectors and explicit rotations:
+    PER_QUERY_G -- row i takes g from its own length i + 1; SLIDING -- keys with
+    i - j >= w are not attended; QUERY_SHIFT -- the aliased query position is
+    floor(i/g) + w - floor(w/g) and g follows the shifted rule.
+    Returns (out [S,Hq,D], lse [Hq,S], exact-RoPE q, k), or None when the
+    shifted rule has no g for some row."""
+    S, Hq, D = qr.shape
+    Hkv = kr.shape[1]
+    grp = Hq // Hkv
+    tau = 1.0 / math.sqrt(D)
+    qx = np.array([[rope_raw(qr[i, h], i, theta) for h in range(Hq)] for i in range(S)])
+    kx = np.array([[rope_raw(kr[j, h], j, theta) for h in range(Hkv)] for j in range(S)])
+    out = np.zeros((S, Hq, D))
+    lse = np.zeros((Hq, S))
+    for i in range(S):
+        s_row = i + 1 if flags & PER_QUERY_G else S
+        if flags & QUERY_SHIFT:
+            g = smallest_group_shift(s_row, L, w)
+            if g is None:
+                return None
+            shift = w - w // g
+        else:
+            g, shift = smallest_group(s_row, L), 0
+        for h in range(Hq):
+            hk = h // grp
+            qa = rope_raw(qr[i, h], i // g + shift, theta)
+            sc, vals = [], []
+            for j in range(i + 1):
+                if i - j < w:
+                    sc.append(tau * qx[i, h] @ kx[j, hk])
+                elif flags & SLIDING:
+                    continue
+                else:
+                    sc.append(tau * qa @ rope_raw(kr[j, hk], j // g, theta))
+                vals.append(vr[j, hk])
+            sc = np.array(sc)
+            m = sc.max()
+            p = np.exp(sc - m)
+            out[i, h] = (p @ np.array(vals)) / p.sum()
+            lse[h, i] = m + math.log(p.sum())
+    return out, lse, qx, kx

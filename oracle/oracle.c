@@ -297,6 +297,139 @@ int oracle_bifocal_rows_3pass(const double *q, const double *k, const double *v,
     return 0;
 }
 
+/* ------------------------------------------------------------------ */
+/* Variants (the method's optional forms, one flag each):              */
+/*                                                                     */
+/*  ORACLE_PER_QUERY_G  query i uses its own current length s = i + 1, */
+/*      so g = g(i + 1) changes inside one prefill (abstract: the      */
+/*      factor adapts to the current length s; a causal model at       */
+/*      token i has seen i + 1 tokens).                                */
+/*  ORACLE_SLIDING      a sliding-window layer of a hybrid model: keys */
+/*      with i - j >= w are not attended at all and no key is aliased  */
+/*      (seventnews.com, "Generalization to hybrid attention           */
+/*      architectures": local-window layers keep their own window).    */
+/*  ORACLE_QUERY_SHIFT  Self-Extend-style shift: the aliased query     */
+/*      position is floor(i/g) + (w - floor(w/g)), which makes the     */
+/*      aliased distance continuous with the exact one at i - j = w;   */
+/*      g is then the smallest integer with                            */
+/*      floor((s-1)/g) + w - floor(w/g) <= L - 1 (ResearchPod summary  */
+/*      names Self-Extend as a baseline; the shift is its grouping).   */
+/* ------------------------------------------------------------------ */
+#define ORACLE_PER_QUERY_G 1
+#define ORACLE_SLIDING 2
+#define ORACLE_QUERY_SHIFT 4
+
+/* Smallest g >= 1 whose largest aliased distance, with the query shifted by
+ * w - floor(w/g), stays inside the pretrained window: literal search.
+ * -1 when no g does (w >= L). */
+int64_t oracle_group_factor_shift(int64_t s, int64_t L, int64_t w)
+{
+    if (s < 1 || L < 1 || w < 1) return -1;
+    int64_t gmax = (s > w ? s : w) + 1;
+    for (int64_t g = 1; g <= gmax; g++)
+        if ((s - 1) / g + (w - w / g) <= L - 1) return g;
+    return -1;
+}
+
+/* g of a row of current length s under the flags (-1: no valid g). */
+int64_t oracle_row_group(int64_t s, int64_t L, int64_t w, int64_t flags)
+{
+    return (flags & ORACLE_QUERY_SHIFT) ? oracle_group_factor_shift(s, L, w)
+                                        : oracle_group_factor(s, L);
+}
+
+/* Single masked pass with variant flags; same layout and result convention as
+ * oracle_bifocal_rows (which this equals when flags == 0).  The grouped keys
+ * are built once per distinct g that some row uses. */
+int oracle_bifocal_rows_ex(const double *q, const double *k, const double *v,
+                           int64_t B, int64_t Sq, int64_t Hq, int64_t Hkv, int64_t Sk,
+                           int64_t D, const int64_t *qpos, int64_t s_len, int64_t L,
+                           int64_t w, double theta, int64_t flags, double *out, double *lse)
+{
+    if (check_args(B, Sq, Hq, Hkv, Sk, D, s_len, L, w, theta)) return -1;
+    if (flags & ~(int64_t)(ORACLE_PER_QUERY_G | ORACLE_SLIDING | ORACLE_QUERY_SHIFT)) return -1;
+    const int64_t grp = Hq / Hkv;
+    const double tau = 1.0 / sqrt((double)D);
+    /* g of every row */
+    int64_t *grow = (int64_t *)malloc((size_t)(Sq > 0 ? Sq : 1) * sizeof(int64_t));
+    if (!grow) return -1;
+    for (int64_t r = 0; r < Sq; r++) {
+        int64_t s_row = (flags & ORACLE_PER_QUERY_G) ? qpos[r] + 1 : s_len;
+        grow[r] = oracle_row_group(s_row, L, w, flags);
+        if (grow[r] < 1) {
+            free(grow);
+            return -1;
+        }
+    }
+    for (int64_t b = 0; b < B; b++) {
+        for (int64_t hk = 0; hk < Hkv; hk++) {
+            /* rows are handled in groups of equal g */
+            int64_t done_g = 0;
+            for (;;) {
+                int64_t g = -1;
+                for (int64_t r = 0; r < Sq; r++)
+                    if (grow[r] > done_g && (g < 0 || grow[r] < g)) g = grow[r];
+                if (g < 0) break;
+                done_g = g;
+                double *kg = grouped_keys(k, b, hk, Sk, Hkv, D, g, theta);
+                if (!kg) {
+                    free(grow);
+                    return -1;
+                }
+                const int64_t shift = (flags & ORACLE_QUERY_SHIFT) ? w - w / g : 0;
+                int64_t nrow = Sq * grp;
+#pragma omp parallel
+                {
+                    double *sc = (double *)malloc((size_t)Sk * sizeof(double));
+                    double *qg = (double *)malloc((size_t)D * sizeof(double));
+                    unsigned char *use = (unsigned char *)malloc((size_t)Sk);
+#pragma omp for schedule(dynamic, 1)
+                    for (int64_t t = 0; t < nrow; t++) {
+                        int64_t r = t / grp, h = hk * grp + t % grp;
+                        if (grow[r] != g) continue;
+                        int64_t i = qpos[r];
+                        const double *qi = q + ((b * Sq + r) * Hq + h) * D;
+                        rotate(qi, qg, D, floor_div(i, g) + shift - i, theta);
+                        int64_t jmax = i < Sk - 1 ? i : Sk - 1;
+                        double m = -INFINITY;
+                        for (int64_t j = 0; j <= jmax; j++) {
+                            const double *kj = k + ((b * Sk + j) * Hkv + hk) * D;
+                            use[j] = 1;
+                            if (i - j < w) {
+                                sc[j] = tau * dot(qi, kj, D);
+                            } else if (flags & ORACLE_SLIDING) {
+                                use[j] = 0; /* outside a sliding window: not attended */
+                                continue;
+                            } else {
+                                sc[j] = tau * dot(qg, kg + j * D, D);
+                            }
+                            if (sc[j] > m) m = sc[j];
+                        }
+                        double *o = out + ((b * Sq + r) * Hq + h) * D;
+                        for (int64_t d = 0; d < D; d++) o[d] = 0.0;
+                        double Z = 0.0;
+                        for (int64_t j = 0; j <= jmax; j++) {
+                            if (!use[j]) continue;
+                            double p = exp(sc[j] - m);
+                            Z += p;
+                            const double *vj = v + ((b * Sk + j) * Hkv + hk) * D;
+                            for (int64_t d = 0; d < D; d++) o[d] += p * vj[d];
+                        }
+                        for (int64_t d = 0; d < D; d++) o[d] /= Z;
+                        lse[(b * Hq + h) * Sq + r] = (jmax >= 0) ? m + log(Z) : -INFINITY;
+                    }
+                    free(sc);
+                    free(qg);
+                    free(use);
+                }
+                free(kg);
+            }
+        }
+    }
+    free(grow);
+    return 0;
+}
+
 /* Number of OpenMP threads the oracle runs on (1 without OpenMP). */
 int oracle_num_threads(void)
 {

@@ -16,6 +16,10 @@ What each pin rests on:
                  (torch scaled_dot_product_attention, fp64)
   all-remote     w = 1 reduces to causal attention at aliased positions
   closed forms   hand-evaluated tiny cases (constant raw vectors)
+  variants       per-query g, sliding window and query shift: brute force from
+                 raw vectors, per-query rows == decodes at their own length,
+                 sliding == band-masked SDPA, the shifted g rule's hand-checked
+                 golden rows (tests/golden/group_factor_shift.txt), a closed form
 """
 from __future__ import annotations
 
@@ -217,5 +221,129 @@ def pin_decode_row(orc):
         _close(l_d[0, :, 0], l_p[0, :, n - 1], 0.0, "decode lse")
 
 
+# ---------------------------------------------------------------- variants
+PQ, SW, SH = 1, 2, 4  # per-query g, sliding window, query shift
+
+
+def pin_variant_group_rule(orc):
+    """Shifted g rule: the hand-checked golden rows, and a pair-by-pair search."""
+    with open(os.path.join(GOLDEN, "group_factor_shift.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            s, L, w, g = map(int, line.split())
+            assert orc.group_factor_shift(s, L, w) == g, (s, L, w, g)
+    for s in range(1, 40):
+        for L in range(1, 14):
+            for w in range(1, 16):
+                want = brute.smallest_group_shift(s, L, w)
+                assert orc.group_factor_shift(s, L, w) == (-1 if want is None else want), (s, L, w)
+
+
+def pin_variant_brute(orc, sizes=range(1, 9), D=4, theta=10.0, seed=23):
+    """Every (L, w) and flag combination on tiny sequences against the raw-vector
+    statement in oracle/brute.py (explicit rotations to aliased positions)."""
+    r = _rng(seed)
+    for S in sizes:
+        qr = r.standard_normal((S, 2, D))
+        kr = r.standard_normal((S, 1, D))
+        vr = r.standard_normal((S, 1, D))
+        for flags in (PQ, SW, SH, PQ | SH):
+            for L in range(1, S + 2):
+                for w in range(1, S + 2):
+                    ref = brute.bifocal_variant_from_raw(qr, kr, vr, L, w, theta, flags)
+                    if ref is None:  # no g for the shifted rule: the oracle refuses too
+                        try:
+                            orc.bifocal_prefill_ex(ref_q(qr, theta), ref_q(kr, theta), vr[None], L, w,
+                                                   theta, flags)
+                        except ValueError:
+                            continue
+                        raise AssertionError(f"variant {flags}: accepted S={S} L={L} w={w}")
+                    out_b, lse_b, qx, kx = ref
+                    out, lse = orc.bifocal_prefill_ex(qx[None], kx[None], vr[None], L, w, theta, flags)
+                    _close(out[0], out_b, 1e-12, f"variant {flags} out S={S} L={L} w={w}")
+                    _close(lse[0], lse_b, 1e-12, f"variant {flags} lse S={S} L={L} w={w}")
+
+
+def ref_q(xr, theta):
+    """Exact-RoPE copy of raw vectors [S,H,D] at positions 0..S-1, batch of one."""
+    return rope_complex(xr, np.arange(xr.shape[0]), theta)[None]
+
+
+def pin_variant_flags_off(orc):
+    """No flag: the variant entry point is the single masked pass, bit for bit."""
+    r = _rng(29)
+    S, D = 90, 8
+    q, k, v = (r.standard_normal((2, S, h, D)) for h in (4, 2, 2))
+    for L, w in ((7, 3), (90, 5), (11, 40)):
+        o0, l0 = orc.bifocal_prefill(q, k, v, L, w, 1.0e4)
+        o1, l1 = orc.bifocal_prefill_ex(q, k, v, L, w, 1.0e4, 0)
+        _close(o1, o0, 0.0, "flags 0 out")
+        _close(l1, l0, 0.0, "flags 0 lse")
+
+
+def pin_per_query_rows_are_decodes(orc):
+    """Per-query g: row i is the decode of the token at i over keys 0..i, whose
+    current length is i + 1 -- and the last row is the ordinary prefill's."""
+    r = _rng(31)
+    S, D = 60, 8
+    q, k, v = (r.standard_normal((1, S, h, D)) for h in (4, 2, 2))
+    for L, w in ((7, 3), (13, 1), (60, 4)):
+        o, l = orc.bifocal_prefill_ex(q, k, v, L, w, 1.0e4, PQ)
+        for i in range(S):
+            od, ld = orc.bifocal_decode(q[:, i:i + 1], k[:, :i + 1], v[:, :i + 1], L, w, 1.0e4)
+            _close(o[0, i], od[0, 0], 1e-13, f"per-query row {i} out L={L} w={w}")
+            _close(l[0, :, i], ld[0, :, 0], 1e-13, f"per-query row {i} lse L={L} w={w}")
+        o_p, l_p = orc.bifocal_prefill(q, k, v, L, w, 1.0e4)
+        _close(o[0, S - 1], o_p[0, S - 1], 1e-13, "per-query last row")
+
+
+def pin_sliding_is_banded_attention(orc):
+    """Sliding window: causal attention restricted to 0 <= i - j < w (torch
+    SDPA with an explicit band mask, fp64); w >= S is plain causal attention."""
+    import torch
+
+    r = _rng(37)
+    S, D = 70, 16
+    q, k, v = (r.standard_normal((S, h, D)) for h in (4, 2, 2))
+    i = torch.arange(S)[:, None]
+    j = torch.arange(S)[None, :]
+    tq = torch.from_numpy(q).permute(1, 0, 2)
+    tk = torch.from_numpy(k).permute(1, 0, 2).repeat_interleave(2, 0)
+    tv = torch.from_numpy(v).permute(1, 0, 2).repeat_interleave(2, 0)
+    for L, w in ((5, 1), (5, 9), (80, 9), (5, 70)):
+        band = (j <= i) & (i - j < w)
+        ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=band)
+        sc = (tq @ tk.transpose(1, 2)) / math.sqrt(D)
+        ref_l = torch.logsumexp(sc.masked_fill(~band, float("-inf")), dim=-1)
+        out, lse = orc.bifocal_prefill_ex(q[None], k[None], v[None], L, w, 1.0e4, SW)
+        _close(out[0], ref.permute(1, 0, 2).numpy(), 1e-12, f"sliding out w={w}")
+        _close(lse[0], ref_l.numpy(), 1e-12, f"sliding lse w={w}")
+
+
+def pin_shift_closed_form(orc):
+    """Query shift with constant raw vectors q~ = k~ = (1, 0), D = 2: an aliased
+    score is tau*cos(floor(i/g) + w - floor(w/g) - floor(j/g)).  S = 8, L = 6,
+    w = 2: g = 2 (g = 1: 7 + 0 > 5; g = 2: 3 + 1 = 4 <= 5), shift 1."""
+    tau = 1.0 / math.sqrt(2.0)
+    S, L, w = 8, 6, 2
+    pos = np.arange(S, dtype=np.float64)
+    q = np.stack([np.cos(pos), np.sin(pos)], axis=-1)[None, :, None, :]
+    v = np.stack([pos, pos * pos], axis=-1)[None, :, None, :]
+    out, lse = orc.bifocal_prefill_ex(q, q.copy(), v, L, w, 1.0e4, SH)
+    for i in range(S):
+        sc = [tau * math.cos(i - j) if i - j < w else tau * math.cos(i // 2 + 1 - j // 2)
+              for j in range(i + 1)]
+        Z = sum(math.exp(x) for x in sc)
+        assert abs(lse[0, 0, i] - math.log(Z)) < 1e-13, i
+        o0 = sum(math.exp(x) * j for j, x in enumerate(sc)) / Z
+        assert abs(out[0, i, 0, 0] - o0) < 1e-13, i
+    # at distance exactly w from an even row the aliased distance is w too:
+    # the shifted view is continuous with the exact one at the window edge
+    assert all((i // 2 + 1 - (i - w) // 2) == w for i in range(w, S, 2))
+
+
 ALL_PINS = [pin_group_rule, pin_rope, pin_brute, pin_three_pass, pin_plain_limits,
-            pin_all_remote, pin_closed_forms, pin_decode_row]
+            pin_all_remote, pin_closed_forms, pin_decode_row, pin_variant_group_rule,
+            pin_variant_brute, pin_variant_flags_off, pin_per_query_rows_are_decodes,
+            pin_sliding_is_banded_attention, pin_shift_closed_form]
