@@ -35,9 +35,9 @@ METRIC = "bifocal prefill attn TFLOP/s @128K (% of BF16 peak); decode µs/token 
 WORKLOAD = dict(B=1, Hq=32, Hkv=8, D=128, S=131072, L_pre=32768, w=4096, theta=1e6, seed=2)
 DECODE_NS = (8192, 32768, 131072)
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
-# DRAM bytes (read + write) of one 128K bifocal prefill launch from the ncu
-# launch list in profiles/launches_bench_prefill128k_decode128k.md, valid only
-# for the prefill source it was measured on (first 16 hex digits of its sha256).
+# DRAM bytes (read + write) of one 128K bifocal prefill launch, from the ncu
+# counters of a one-launch capture, valid only for the prefill source they were
+# measured on (first 16 hex digits of its sha256).
 PREFILL_TRAFFIC = {"sha256_16": "42ec6803786d95ff", "bytes": 3.554e9 + 1.058e9}
 
 
@@ -48,6 +48,12 @@ def prefill_traffic():
     with open(path, "rb") as f:
         h = hashlib.sha256(f.read()).hexdigest()[:16]
     return PREFILL_TRAFFIC["bytes"] if h == PREFILL_TRAFFIC["sha256_16"] else None
+
+
+def prefill_kernel_name(grp, D):
+    """The tile kernel libjetlong dispatches to by default: one CTA per query
+    tile of two heads of a GQA group (one when the group size is odd)."""
+    return f"prefill_kernel<{D},{2 if grp % 2 == 0 else 1}>"
 
 
 def prefill_flops(B, Hq, D, S):
@@ -65,9 +71,23 @@ def load_peaks():
     try:
         with open(path) as f:
             d = json.load(f)
-        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+        peaks = {k: float(d[k]) for k in FALLBACK_PEAKS}
+        # SM clock the sustained (power-capped, back-to-back) GEMM loop settled at
+        mhz = (d.get("clocks_under_load") or {}).get("sm_mhz_median")
+        peaks["sustained_sm_mhz"] = float(mhz) if mhz else None
+        return peaks, "measured"
     except (OSError, KeyError, ValueError):
-        return dict(FALLBACK_PEAKS), "fallback"
+        return dict(FALLBACK_PEAKS, sustained_sm_mhz=None), "fallback"
+
+
+def sustained_frac_at_clock(achieved, peaks, kernel_mhz):
+    """achieved / (the sustained GEMM rate per MHz x the kernel's own median SM
+    clock): the sustained peak was taken at the clock a power-capped cuBLAS loop
+    settles to, so it is rescaled to the clock this kernel actually ran at."""
+    mhz0 = peaks.get("sustained_sm_mhz")
+    if not mhz0 or not kernel_mhz:
+        return None
+    return achieved / (peaks["bf16_tflops_sustained"] / mhz0 * kernel_mhz)
 
 
 # ------------------------------------------------------------------ clocks
@@ -203,6 +223,24 @@ def run_ours(args, rank, world, dev):
     plain_ms = time_calls(lambda: jl.jl_bifocal_prefill(q, k, v, S, w, theta, out=out, lse=lse,
                                                         stream=stream), stream, dev, reps=max(3, args.steps))
     decode = decode_sweep(jl, dev, stream, peaks)
+    # the method's optional forms on the same 128K layer (same FLOP convention)
+    variants = {}
+    for name, flags in (("per_query_g", jl.JL_VARIANT_PER_QUERY_G), ("sliding_window", jl.JL_VARIANT_SLIDING),
+                        ("query_shift", jl.JL_VARIANT_QUERY_SHIFT)):
+        v_ms = time_calls(lambda f=flags: jl.jl_bifocal_prefill_ex(q, k, v, 0, L, w, theta, f, out=out, lse=lse,
+                                                                   stream=stream), stream, dev, reps=3)
+        variants[name] = {"ms": round(v_ms, 3), "tflops_causal_convention": round(flops / (v_ms * 1e-3) / 1e12, 2),
+                          "g": jl.jl_group_factor_ex(S, L, w, flags)}
+    variants["sliding_window"]["note"] = "attends only the last w keys: FLOPs counted on the full causal convention"
+    # the two-SM tile kernel (cta_group::2), opt-in: bifocal and plain on the same layer
+    pair = {}
+    for tag, L_pre in (("bifocal", L), ("plain", S)):
+        pair[tag + "_ms"] = round(time_calls(lambda Lp=L_pre: jl.jl_bifocal_prefill_ex(
+            q, k, v, 0, Lp, w, theta, jl.JL_PREFILL_CTA_PAIR, out=out, lse=lse, stream=stream), stream, dev, reps=3), 3)
+    pair["bifocal_overhead"] = round(pair["bifocal_ms"] / pair["plain_ms"] - 1.0, 4)
+    pair["tflops"] = round(flops / (pair["bifocal_ms"] * 1e-3) / 1e12, 2)
+    if jl.jl_debug_status() != 0:
+        raise RuntimeError("device status word set by the variant runs")
     # chunked prefill: the last 8K tokens of the same context over the cache of
     # the first 120K (same k / v buffers as the cache), s = S as above
     S_new = 8192
@@ -239,6 +277,8 @@ def run_ours(args, rank, world, dev):
         "plain_rope": {"tflops": round(flops / (plain_ms * 1e-3) / 1e12, 2), "ms": round(plain_ms, 3),
                        "bifocal_overhead": round(avg_prefill_ms / plain_ms - 1.0, 4)},
         "decode": decode,
+        "variants": variants,
+        "prefill_cta_pair": pair,
         "paged_decode": paged,
         "rope_cache_write": {"rows": S, "us": round(1e3 * cw_ms, 2),
                              "gbs": round(cw_bytes / (cw_ms * 1e-3) / 1e9, 1),
@@ -249,17 +289,21 @@ def run_ours(args, rank, world, dev):
         "decode_in_step_us": round(1e3 * sum(decode_ms) / len(decode_ms), 2),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
-                     "traffic": prefill_traffic(), "kernel": "prefill_kernel<128,2>",
+                     "traffic": prefill_traffic(), "kernel": prefill_kernel_name(Hq // Hkv, D),
                      "peak_source": f"{peaks_src} bf16 burst",
-                     # also reported: the back-to-back cuBLAS figure, taken at the
-                     # power-capped clock that loop settles to (this kernel runs
-                     # at higher clocks, so `frac` against the burst peak is the
-                     # conservative headline)
+                     # also reported: the back-to-back cuBLAS figure rescaled from
+                     # the clock its power-capped loop settled at to this kernel's
+                     # median clock over the timed steps (same work per cycle)
                      "sustained_peak": peaks["bf16_tflops_sustained"],
-                     "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4)},
-        "gpu_launches": 2 * args.steps,
+                     "sustained_peak_sm_mhz": peaks.get("sustained_sm_mhz"),
+                     "frac_of_sustained_at_kernel_clock": None},
+        # per step: the prefill tile kernel, its fp32 pass over the rows below
+        # position 256, and the decode kernel
+        "gpu_launches": 3 * args.steps,
         "clocks": clk.summary(),
     }
+    f_s = sustained_frac_at_clock(achieved, peaks, res["clocks"].get("sm_mhz"))
+    res["roofline"]["frac_of_sustained_at_kernel_clock"] = None if f_s is None else round(f_s, 4)
     if not args.no_e2e:
         res["e2e"] = e2e(jl, args, dev, stream)
     if rank == 0 and not args.no_cpu:

@@ -72,7 +72,9 @@ typedef enum {
     JL_ERR_CUDA = -5,        /* a CUDA runtime call or launch failed             */
     JL_ERR_TIMEOUT = -6,     /* device status only: a bounded wait expired       */
     JL_ERR_WORKSPACE = -7,   /* workspace pointer NULL or smaller than required  */
-    JL_ERR_GUARD = -8        /* device status only: an in-kernel guard fired     */
+    JL_ERR_GUARD = -8        /* device status only: an in-kernel guard fired (a
+                                non-finite score, a length or page id out of
+                                range); see the entry points                   */
 } jl_status;
 
 /* Human-readable name of a jl_status value (static string, never NULL). */
@@ -92,6 +94,52 @@ const char *jl_version(void);
  * (g would not fit in int32).
  */
 int jl_group_factor(int64_t s, int64_t L_pre, int32_t *g_out);
+
+/*
+ * Variant flags of the _ex entry points (the method's optional forms).
+ *   JL_VARIANT_PER_QUERY_G  query i uses its own current length s = i + 1, so
+ *       g = g(i + 1, L_pre) grows inside one prefill (abstract: the factor
+ *       adapts to the current length s; a causal model at token i has seen
+ *       i + 1 tokens).  A decode's single query already has s = n.
+ *   JL_VARIANT_SLIDING  a sliding-window layer of a hybrid model: keys with
+ *       i - j >= w are not attended and nothing is aliased (seventnews.com,
+ *       "Generalization to hybrid attention architectures": local-window
+ *       layers keep their own window); L_pre plays no part.  Must come alone.
+ *   JL_VARIANT_QUERY_SHIFT  Self-Extend-style grouping (the ResearchPod
+ *       summary names Self-Extend as a baseline): the aliased query position
+ *       is floor(i/g) + w - floor(w/g), which makes aliased distances continue
+ *       the exact ones at i - j = w, and g = g_shift(s, L_pre, w) is the
+ *       smallest integer with floor((s-1)/g) + w - floor(w/g) <= L_pre - 1
+ *       (see jl_group_factor_ex).  For s > L_pre it needs w < L_pre.
+ * Prefill accepts PER_QUERY_G and QUERY_SHIFT one at a time
+ * (JL_ERR_UNSUPPORTED for both together).
+ */
+#define JL_VARIANT_PER_QUERY_G 1u
+#define JL_VARIANT_SLIDING 2u
+#define JL_VARIANT_QUERY_SHIFT 4u
+
+/*
+ * Kernel choice of jl_bifocal_prefill_ex (combines with the variant flags):
+ * JL_PREFILL_CTA_PAIR runs, where it applies (D = 128 and Hq / Hkv a multiple
+ * of 4), the two-SM tile kernel: a cluster of two CTAs per query tile of four
+ * heads, tcgen05 MMAs of M = 256 across both SMs (cta_group::2), each CTA
+ * loading and correcting half of every K tile.  It computes the same result
+ * (parity-tested like the default) with half the correction work per SM, but
+ * each tile's softmax -> MMA handshake then crosses SMs; on B300 it measured
+ * 151 ms bifocal / 137 ms plain at the 128K Qwen3-8B-shaped layer against
+ * 137 / 114 ms for the default one-CTA kernel, so it is not the default.
+ * Elsewhere the flag is ignored.
+ */
+#define JL_PREFILL_CTA_PAIR 8u
+
+/*
+ * Group factor under variant flags -- host, pure.  Without JL_VARIANT_QUERY_SHIFT
+ * it is jl_group_factor(s, L_pre) (w unused); with it, g_shift(s, L_pre, w) as
+ * defined above.  JL_VARIANT_SLIDING gives 1 (nothing is aliased).
+ * Returns JL_OK, JL_ERR_ARG (s, L_pre or w < 1, an unknown flag, g_out NULL, or
+ * no g for the shifted rule) or JL_ERR_OVERFLOW.
+ */
+int jl_group_factor_ex(int64_t s, int64_t L_pre, int64_t w, unsigned flags, int32_t *g_out);
 
 /*
  * Exact RoPE, in place: x[b, s, h, :] <- R_{pos0 + s}(x[b, s, h, :]).
@@ -126,7 +174,18 @@ int jl_rope_cache_write(const void *k_raw, const void *v, void *k_cache, void *v
                         int S_new, int H, int D, int n_past, int n_cap, double theta, void *stream);
 
 /*
- * Bifocal causal GQA prefill attention (one TMA + tcgen05 kernel).
+ * Bifocal causal GQA prefill attention (a TMA + tcgen05 tile kernel).
+ * Numerics: the exact view multiplies the bf16 inputs as they are; the remote
+ * view multiplies the corrected q and k rounded to fp16 (11-bit significand,
+ * so one remote score carries a rounding error of about 4e-4 that the softmax
+ * averages over the row's keys).  The rotation keeps each pair's norm, so
+ * inputs whose elements all lie below 46000 in magnitude give finite fp16
+ * operands; a score that is not finite is reported as JL_ERR_GUARD in the
+ * device status word.  Rows at positions below 256 that have remote keys
+ * (g > 1 and w < 256) see too few keys for that averaging: a second, CUDA-core
+ * kernel recomputes exactly those rows in fp32 after the tile kernel.
+ * out is normalised by the sum of P as rounded to bf16 for P.V (so it is a
+ * weighted mean of V rows); lse uses the fp32 sum.
  * The three attention passes of the pages -- local(window, exact RoPE),
  * remote(all, aliased) and remote(window, aliased), merged by
  * inclusion-exclusion on log-sum-exp statistics (ResearchPod transcript on
@@ -173,6 +232,22 @@ int jl_bifocal_prefill_chunk(const void *q, const void *k_cache, const void *v_c
                              int D, int L_pre, int w, double theta, void *stream);
 
 /*
+ * jl_bifocal_prefill_chunk with variant flags (JL_VARIANT_*; 0 gives exactly
+ * jl_bifocal_prefill_chunk, and n_past = 0, n_cap = S_new a full prefill).
+ * PER_QUERY_G runs one launch per range of rows that share g -- the rows
+ * [(g-1) L_pre, g L_pre) -- each scored as the chunk of a prefill of length
+ * g L_pre.  SLIDING visits only the key tiles the window reaches.
+ * QUERY_SHIFT shifts the query's correction offset by w - floor(w/g).
+ * JL_PREFILL_CTA_PAIR selects the two-SM tile kernel (see above).
+ * Returns what jl_bifocal_prefill_chunk returns; JL_ERR_ARG also for an unknown
+ * flag, SLIDING with another variant flag, or a QUERY_SHIFT with no valid g;
+ * JL_ERR_UNSUPPORTED for PER_QUERY_G with QUERY_SHIFT.
+ */
+int jl_bifocal_prefill_ex(const void *q, const void *k_cache, const void *v_cache, void *out,
+                          float *lse, int B, int Hq, int Hkv, int S_new, int n_past, int n_cap,
+                          int D, int L_pre, int w, double theta, unsigned flags, void *stream);
+
+/*
  * Workspace bytes jl_bifocal_decode needs for these sizes (split-KV partial
  * statistics and one arrival counter per (batch, kv head)).  The value does
  * not grow with n: a workspace sized once serves every cache length for the
@@ -181,7 +256,12 @@ int jl_bifocal_prefill_chunk(const void *q, const void *k_cache, const void *v_c
 size_t jl_bifocal_decode_workspace_size(int B, int Hq, int Hkv, int n, int D);
 
 /*
- * Bifocal single-token decode over an exact-RoPE bf16 KV cache (split-KV).
+ * Bifocal single-token decode over an exact-RoPE bf16 KV cache (split-KV,
+ * fp32 arithmetic on CUDA cores; a non-finite score is reported as
+ * JL_ERR_GUARD in the device status word).
+ * Kernels exist for GQA group sizes Hq / Hkv in {1, 2, 4, 8}; any other group
+ * size returns JL_ERR_UNSUPPORTED (this also holds for the paged and the
+ * no-allocation variants).
  * The cache keeps original positions and is never rewritten; remote keys are
  * corrected at lookup time (ResearchPod transcript on the cache; abstract:
  * at most ~4% generation overhead).  The query is the token at position n-1
@@ -204,6 +284,20 @@ int jl_bifocal_decode(const void *q, const void *k_cache, const void *v_cache, v
                       int w, double theta, void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * jl_bifocal_decode with variant flags (JL_VARIANT_*; 0 gives exactly
+ * jl_bifocal_decode).  PER_QUERY_G changes nothing for the single query at
+ * n - 1 (its length is n).  SLIDING attends to the last min(n, w) keys only,
+ * all exact.  QUERY_SHIFT uses g_shift(n, L_pre, w) and shifts the query's
+ * correction offset by w - floor(w/g).  Same workspace as jl_bifocal_decode.
+ * Returns what jl_bifocal_decode returns; JL_ERR_ARG also for an unknown flag,
+ * SLIDING with another flag, or a QUERY_SHIFT with no valid g.
+ */
+int jl_bifocal_decode_ex(const void *q, const void *k_cache, const void *v_cache, void *out,
+                         float *lse, int B, int Hq, int Hkv, int n, int n_cap, int D, int L_pre,
+                         int w, double theta, unsigned flags, void *workspace, size_t ws_bytes,
+                         void *stream);
+
+/*
  * Bifocal decode of a batch of sequences of different lengths over a paged
  * KV cache: sequence b has n_b = seq_lens[b] tokens, its query is the token at
  * position n_b - 1, and it sets its own g = g(n_b, L_pre) -- the group factor
@@ -214,7 +308,9 @@ int jl_bifocal_decode(const void *q, const void *k_cache, const void *v_cache, v
  *   q        device bf16 [B, Hq, D], exact RoPE at each sequence's position n_b - 1
  *   k_pages, v_pages  device bf16 [num_pages, page_size, Hkv, D], exact RoPE
  *   block_table  device int32 [B, max_pages]; entries past a sequence's last
- *            page are never read; an id outside [0, num_pages) reads zeros
+ *            page are never read; an id that a sequence uses but that lies
+ *            outside [0, num_pages) reads zeros (never faults) and is reported
+ *            as JL_ERR_GUARD in the device status word
  *   seq_lens device int32 [B], 1 <= n_b <= max_n; a length outside that range
  *            is clamped into it and reported as JL_ERR_GUARD in the device
  *            status word (the call never reads past the table or the plan)

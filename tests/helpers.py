@@ -36,46 +36,21 @@ def bf16_to_f64(t) -> np.ndarray:
     return t.detach().to("cpu").to(torch.float64).numpy()
 
 
-# Edge cases outside the benchmark configurations whose rows hold only a
-# handful of keys, most of them remote (w = 1): there the log-sum-exp carries
-# the rounding of single scores undamped.  The remote view multiplies q and k
-# corrected and rounded to fp16 (relative error u = 2^-11 each), so one score
-# errs by tau * sum_d q_d k_d (e_q + e_k), whose standard deviation for
-# unit-variance data is tau * u * sqrt(2/3) * sqrt(D) = u * sqrt(2/3) ~ 4.0e-4
-# at any D; such cases hold lse to five of those, absolutely.
-def lse_abs_tol_few_remote_keys(D):
-    return 5.0 * 2.0 ** -11 * (2.0 / 3.0) ** 0.5
-
-
-def bf16_ulp(x):
-    """Spacing of bf16 numbers at |x| (2^(e-7) for |x| in [2^e, 2^(e+1)))."""
-    a = np.maximum(np.abs(np.asarray(x, dtype=np.float64)), 2.0 ** -126)
-    return 2.0 ** (np.floor(np.log2(a)) - 7)
-
-
-def compare(out_gpu, lse_gpu, out_ref, lse_ref, what="", lse_abs=None):
-    """Assert the parity bar: bf16 out max|d| <= max(1e-2, one bf16 ulp of the
-    reference) and mean|d| <= 1e-3,
+def compare(out_gpu, lse_gpu, out_ref, lse_ref, what=""):
+    """Assert the parity bar: bf16 out max|d| <= 1e-2 and mean|d| <= 1e-3,
     fp32 lse relative error <= 1e-4, taken against max(|lse|, 1) so rows whose
-    log-sum-exp crosses zero are held to 1e-4 absolutely.  ``lse_abs``
-    replaces the lse bar by an absolute one (see lse_abs_tol_few_remote_keys).
-    Returns the measured errors."""
+    log-sum-exp crosses zero are held to 1e-4 absolutely.  Returns the
+    measured errors."""
     d = np.abs(np.asarray(out_gpu, dtype=np.float64) - out_ref)
     mean = float(d.mean())
-    # bf16 outputs: the max-abs bar is 1e-2, or one bf16 ulp of the reference
-    # where that ulp is larger (|ref| >= 2.56, rows of a handful of keys whose
-    # output is not averaged down: bf16 cannot resolve them to 1e-2)
-    mx = float(np.max(d / np.maximum(1.0, bf16_ulp(out_ref) / OUT_MAX_ABS)))
+    mx = float(d.max())
     lse_gpu = np.asarray(lse_gpu, dtype=np.float64)
     dl = np.abs(lse_gpu - lse_ref)
     rel = float(np.max(dl / np.maximum(np.abs(lse_ref), 1.0)))
     assert np.all(np.isfinite(out_gpu)), f"{what}: non-finite output"
     assert mx <= OUT_MAX_ABS, f"{what}: out max abs err {mx:.3e}"
     assert mean <= OUT_MEAN_ABS, f"{what}: out mean abs err {mean:.3e}"
-    if lse_abs is None:
-        assert rel <= LSE_REL, f"{what}: lse rel err {rel:.3e}"
-    else:
-        assert float(dl.max()) <= lse_abs, f"{what}: lse abs err {float(dl.max()):.3e} > {lse_abs:.2e}"
+    assert rel <= LSE_REL, f"{what}: lse rel err {rel:.3e}"
     return mx, mean, rel
 
 

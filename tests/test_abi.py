@@ -68,6 +68,56 @@ def test_group_factor_rejects(jl):
     assert g.value == 7
 
 
+def test_group_factor_variants(jl, orc):
+    """The query-shift rule against the oracle's literal search and the
+    hand-checked golden rows; per-query g is the plain rule; sliding gives 1."""
+    PQ, SW, SH = jl.JL_VARIANT_PER_QUERY_G, jl.JL_VARIANT_SLIDING, jl.JL_VARIANT_QUERY_SHIFT
+    g = ctypes.c_int32(0)
+    for s in list(range(1, 200, 7)) + [2048, 65536, 131072]:
+        for L in (1, 3, 7, 100, 512, 4096, 32768):
+            for w in (1, 2, 5, 64, 128, 4096):
+                want = orc.group_factor_shift(s, L, w)
+                rc = jl.lib.jl_group_factor_ex(s, L, w, SH, ctypes.byref(g))
+                if want < 0:
+                    assert rc == jl.JL_ERR_ARG, (s, L, w)
+                else:
+                    assert rc == 0 and g.value == want, (s, L, w, g.value, want)
+                assert jl.jl_group_factor_ex(s, L, w, PQ) == orc.group_factor(s, L)
+                assert jl.jl_group_factor_ex(s, L, w, SW) == 1
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "group_factor_shift.txt")
+    for line in open(path):
+        if line.startswith("#") or not line.strip():
+            continue
+        s, L, w, want = map(int, line.split())
+        rc = jl.lib.jl_group_factor_ex(s, L, w, SH, ctypes.byref(g))
+        assert (rc == jl.JL_ERR_ARG) if want < 0 else (rc == 0 and g.value == want), (s, L, w)
+    assert jl.lib.jl_group_factor_ex(5, 4, 2, 8, ctypes.byref(g)) == jl.JL_ERR_ARG  # unknown flag
+    assert jl.lib.jl_group_factor_ex(5, 4, 2, SW | SH, ctypes.byref(g)) == jl.JL_ERR_ARG
+    assert jl.lib.jl_group_factor_ex(5, 4, 0, 0, ctypes.byref(g)) == jl.JL_ERR_ARG
+
+
+def test_variant_entry_points_reject_bad_flags(jl):
+    """Flag errors come back before any launch."""
+    PQ, SW, SH = jl.JL_VARIANT_PER_QUERY_G, jl.JL_VARIANT_SLIDING, jl.JL_VARIANT_QUERY_SHIFT
+
+    def pf(flags, S=256, L=128, w=64):
+        return jl.lib.jl_bifocal_prefill_ex(GOOD, GOOD, GOOD, GOOD, GOOD, 1, 4, 2, S, 0, S, 128, L, w,
+                                            1e4, flags, None)
+
+    def dc(flags, n=256, L=128, w=64):
+        return jl.lib.jl_bifocal_decode_ex(GOOD, GOOD, GOOD, GOOD, GOOD, 1, 32, 8, n, n, 128, L, w, 1e6,
+                                           flags, GOOD, 1 << 30, None)
+
+    assert pf(16) == jl.JL_ERR_ARG
+    assert pf(SW | PQ) == jl.JL_ERR_ARG
+    assert pf(SW | SH) == jl.JL_ERR_ARG
+    assert pf(PQ | SH) == jl.JL_ERR_UNSUPPORTED
+    assert pf(SH, S=256, L=128, w=128) == jl.JL_ERR_ARG  # w >= L: no shifted g
+    assert dc(16) == jl.JL_ERR_ARG
+    assert dc(SW | PQ) == jl.JL_ERR_ARG
+    assert dc(SH, n=256, L=128, w=200) == jl.JL_ERR_ARG
+
+
 def _prefill(jl, q=GOOD, k=GOOD, v=GOOD, out=GOOD, lse=GOOD, B=1, Hq=4, Hkv=2, S=256, D=128,
              L=128, w=64, theta=1e4):
     return jl.lib.jl_bifocal_prefill(q, k, v, out, lse, B, Hq, Hkv, S, D, L, w, theta, None)

@@ -80,3 +80,21 @@ def test_paged_decode_clamps_a_length_past_the_plan(jl, dev):
     assert jl.jl_debug_status() == jl.JL_ERR_GUARD
     assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
     assert jl.jl_debug_status() == 0  # the query cleared it
+
+
+def test_paged_decode_reports_a_page_id_outside_the_pool(jl, dev):
+    """A block-table entry that a sequence uses but that names no page of the
+    pool reads zeros (never faults) and is reported as JL_ERR_GUARD."""
+    import torch
+
+    B, Hq, Hkv, D, P = 1, 8, 2, 128, 64
+    q = torch.ones((B, Hq, D), dtype=torch.bfloat16, device=dev)
+    pages = torch.ones((4, P, Hkv, D), dtype=torch.bfloat16, device=dev)
+    table = torch.tensor([[0, 9]], dtype=torch.int32, device=dev)  # page 9 of a 4-page pool
+    lens = torch.tensor([100], dtype=torch.int32, device=dev)       # uses both table entries
+    jl.jl_bifocal_decode_paged(q, pages, pages, table, lens, 128, 64, 32, 1e6)
+    assert jl.jl_debug_status() == jl.JL_ERR_GUARD
+    assert jl.jl_debug_status() == 0
+    table_ok = torch.tensor([[0, 3]], dtype=torch.int32, device=dev)
+    jl.jl_bifocal_decode_paged(q, pages, pages, table_ok, lens, 128, 64, 32, 1e6)
+    assert jl.jl_debug_status() == 0

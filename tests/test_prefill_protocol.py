@@ -287,3 +287,196 @@ def test_model_finds_the_race_without_the_last_arrival_wait():
             except Race:
                 found += 1
     assert found > 0
+
+
+# ---------------------------------------------------------------- the pair kernel
+def run_pair(S, w, g, qt, NK, NV, seed, last_arrival_waits=True):
+    """prefill_pair_kernel: two CTAs (ranks 0, 1) of one cluster, two heads
+    each.  Each CTA's producers load its own half of every K / V tile; the
+    correction warps of each CTA correct their own K half; the issuer (rank 0)
+    waits on rank 0's K0READY / GO / PFULL1, which count one arrival per warp of
+    BOTH CTAs, and each commit arrives on the barrier of both CTAs.  The last
+    correction arrival of each CTA waits on its own KEMPTY for QK(T - NK)."""
+    rnd = random.Random(seed)
+    NR, T = visit(qt, S, w, g)
+    B = [{}, {}]
+
+    def bar(r, name, count):
+        B[r][name] = Bar(f"{name}@{r}", count)
+
+    for r in range(2):
+        bar(r, "QFULL", 1), bar(r, "K0READY", 8), bar(r, "QFREE", 1)
+        for s in range(NK):
+            bar(r, f"KFULL{s}", 1), bar(r, f"KEMPTY{s}", 1), bar(r, f"GO{s}", 18)
+        for s in range(NV):
+            bar(r, f"VFULL{s}", 1), bar(r, f"VEMPTY{s}", 1)
+        for n in range(2):
+            bar(r, f"SFULL{n}", 1), bar(r, f"PFULL{n}", 8), bar(r, f"ODONE{n}", 1)
+    st = [{"Q": None, "K": [None] * NK, "V": [None] * NV, "S": [None, None], "P": [None, None],
+           "O": [[], []]} for _ in range(2)]
+    tma, pipe = [], []
+
+    def wait(r, name, parity):
+        while not B[r][name].ready(parity):
+            yield "blocked"
+
+    def kprod(r):
+        B[r]["QFULL"].arrive_expect_tx()
+        tma.append((r, "QFULL", lambda: st[r].__setitem__("Q", "exact")))
+        for v in range(T):
+            if v == NR and NR > 0:
+                yield from wait(r, "QFREE", 0)
+                B[r]["QFULL"].arrive_expect_tx()
+                tma.append((r, "QFULL", lambda: st[r].__setitem__("Q", "reloaded")))
+            sk = v % NK
+            yield from wait(r, f"KEMPTY{sk}", ((v // NK) & 1) ^ 1)
+            B[r][f"KFULL{sk}"].arrive_expect_tx()
+            tma.append((r, f"KFULL{sk}", lambda sk=sk, v=v: st[r]["K"].__setitem__(sk, (v, "raw"))))
+            yield "step"
+
+    def vprod(r):
+        for v in range(T):
+            sv = v % NV
+            yield from wait(r, f"VEMPTY{sv}", ((v // NV) & 1) ^ 1)
+            B[r][f"VFULL{sv}"].arrive_expect_tx()
+            tma.append((r, f"VFULL{sv}", lambda sv=sv, v=v: st[r]["V"].__setitem__(sv, v)))
+            yield from wait(r, f"VFULL{sv}", (v // NV) & 1)
+            B[0][f"GO{v % NK}"].arrive()
+            yield "step"
+
+    def correction(r):
+        yield from wait(r, "QFULL", 0)
+        if NR > 0:
+            st[r]["Q"] = "corrected"
+        for u in range(T + 1):
+            if u < T:
+                sk = u % NK
+                yield from wait(r, f"KFULL{sk}", (u // NK) & 1)
+                if st[r]["K"][sk] != (u, "raw"):
+                    raise Race(f"correction@{r}: K stage {sk} holds {st[r]['K'][sk]}, not K({u})")
+                if u < NR:
+                    st[r]["K"][sk] = (u, "corrected")
+                if u == NR and NR > 0:
+                    yield from wait(r, "QFULL", 1)
+            if u == T and last_arrival_waits and T - 1 >= NK:
+                yield from wait(r, f"KEMPTY{(T - NK) % NK}", ((T - NK) // NK) & 1)
+            for _ in range(4):  # one arrival per correction warp
+                B[0]["K0READY" if u == 0 else f"GO{(u - 1) % NK}"].arrive()
+            yield "step"
+
+    def qk_op(v, n):
+        def run():
+            for r in range(2):
+                want = (v, "corrected" if v < NR else "raw")
+                if st[r]["K"][v % NK] != want:
+                    raise Race(f"QK{n}({v}): K half @{r} holds {st[r]['K'][v % NK]}, wants {want}")
+                q_want = "corrected" if v < NR else ("reloaded" if NR > 0 else "exact")
+                if st[r]["Q"] != q_want:
+                    raise Race(f"QK{n}({v}): Q @{r} is {st[r]['Q']}, wants {q_want}")
+                if st[r]["P"][n] not in (None, "consumed"):
+                    raise Race(f"QK{n}({v}): overwrites P{n}@{r} before its PV")
+                st[r]["S"][n], st[r]["P"][n] = v, None
+        return run
+
+    def pv_op(v, n):
+        def run():
+            for r in range(2):
+                if st[r]["V"][v % NV] != v:
+                    raise Race(f"PV{n}({v}): V half @{r} holds {st[r]['V'][v % NV]}")
+                if st[r]["P"][n] != v:
+                    raise Race(f"PV{n}({v}): P{n}@{r} holds {st[r]['P'][n]}")
+                st[r]["P"][n] = "consumed"
+                st[r]["O"][n].append(v)
+        return run
+
+    def issuer():
+        yield from wait(0, "K0READY", 0)
+
+        def qk(v, n):
+            pipe.append(("mma", qk_op(v, n)))
+            pipe.append(("commit", f"SFULL{n}"))
+            if n == 1:
+                pipe.append(("commit", f"KEMPTY{v % NK}"))
+                if v == NR - 1:
+                    pipe.append(("commit", "QFREE"))
+        for n in range(2):
+            qk(0, n)
+        for v in range(T):
+            for n in range(2):
+                yield from wait(0, f"GO{v % NK}" if n == 0 else "PFULL1", (v // NK) & 1 if n == 0 else v & 1)
+                pipe.append(("mma", pv_op(v, n)))
+                pipe.append(("commit", f"ODONE{n}"))
+                if n == 1:
+                    pipe.append(("commit", f"VEMPTY{v % NV}"))
+                if v + 1 < T:
+                    qk(v + 1, n)
+                yield "step"
+
+    def softmax(r, n):
+        for v in range(T):
+            yield from wait(r, f"SFULL{n}", v & 1)
+            if st[r]["S"][n] != v:
+                raise Race(f"softmax{n}@{r}({v}): S holds {st[r]['S'][n]}")
+            st[r]["P"][n] = v
+            for _ in range(4):  # one arrival per softmax warp
+                B[0][f"GO{v % NK}" if n == 0 else "PFULL1"].arrive()
+            yield "step"
+        yield from wait(r, f"ODONE{n}", (T - 1) & 1)
+        if st[r]["O"][n] != list(range(T)):
+            raise Race(f"epilogue{n}@{r}: O accumulated {st[r]['O'][n]}")
+
+    roles = {"issuer": issuer()}
+    for r in range(2):
+        roles.update({f"kprod{r}": kprod(r), f"vprod{r}": vprod(r), f"correction{r}": correction(r),
+                      f"softmax0@{r}": softmax(r, 0), f"softmax1@{r}": softmax(r, 1)})
+    weight = {k: rnd.choice([0.05, 1.0, 20.0]) for k in list(roles) + ["tma", "pipe"]}
+    idle = 0
+    while roles or tma or pipe:
+        choices = list(roles) + (["tma"] if tma else []) + (["pipe"] if pipe else [])
+        choices.sort(key=lambda c: -rnd.random() ** (1.0 / weight[c]))
+        moved = False
+        for c in choices:
+            if c == "tma":
+                r, name, land = tma.pop(rnd.randrange(len(tma)) if rnd.random() < 0.3 else 0)
+                land()
+                B[r][name].complete_tx()
+            elif c == "pipe":
+                kind, x = pipe.pop(0)
+                if kind == "mma":
+                    x()
+                else:  # commits arrive on the barrier of both CTAs
+                    B[0][x].arrive()
+                    B[1][x].arrive()
+            else:
+                try:
+                    if next(roles[c]) == "blocked":
+                        continue
+                except StopIteration:
+                    del roles[c]
+            moved = True
+            break
+        idle = 0 if moved else idle + 1
+        if idle > 3:
+            raise Race(f"deadlock: {sorted(roles)} blocked (NR={NR}, T={T})")
+
+
+@pytest.mark.parametrize("S,L,w", SHAPES)
+def test_pair_protocol_model_has_no_race_or_deadlock(S, L, w):
+    g = _group_factor(S, L)
+    for qt in range(-(-S // KBM)):
+        for seed in range(8):
+            run_pair(S, w, g, qt, 4, 4, seed)
+
+
+def test_pair_model_finds_the_race_without_the_last_arrival_wait():
+    """Planted mistake: without the KEMPTY wait, a CTA's last correction
+    arrival can complete a GO phase early (a PV or QK then reads a stage that
+    is not ready)."""
+    found = 0
+    for qt in range(2, 8):
+        for seed in range(30):
+            try:
+                run_pair(3000, 300, 6, qt, 4, 4, seed, last_arrival_waits=False)
+            except Race:
+                found += 1
+    assert found > 0

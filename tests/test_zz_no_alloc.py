@@ -50,9 +50,15 @@ def test_noalloc_matches_workspace_decode_twice(jl, dev, B, Hq, Hkv, n, n_cap, D
     for call in range(2):
         out = torch.full_like(q, float("nan"))
         lse = torch.full((B, Hq), float("nan"), dtype=torch.float32, device=dev)
+        torch.cuda.synchronize()
+        free_before = torch.cuda.mem_get_info(dev)[0]
         rc = _noalloc(jl, q, k, v, out, lse, n, L, w, theta)
         assert rc == 0, jl.status_string(rc)
         torch.cuda.synchronize()
+        if call == 1:
+            # the first call may load the library's module onto the device and
+            # look up the scratch address; after that a call takes no device memory
+            assert torch.cuda.mem_get_info(dev)[0] == free_before
         helpers.compare(helpers.bf16_to_f64(out), lse.cpu().numpy(), ref_o, ref_l,
                         f"no-alloc decode call {call} n={n}")
     assert jl.jl_debug_status() == 0
@@ -72,3 +78,24 @@ def test_noalloc_rejects_shapes_beyond_its_scratch(jl, dev):
     rc = jl.lib.jl_bifocal_decode_noalloc(_ptr(q), _ptr(kv), _ptr(kv), _ptr(out), _ptr(lse), B, Hq,
                                           Hkv, n, n, D, 32768, 4096, 1e6, stream)
     assert rc == jl.JL_ERR_WORKSPACE
+
+
+def test_noalloc_rejects_unsupported_and_misaligned_arguments(jl, dev):
+    """Argument errors the workspace entry point reports (an unsupported GQA
+    group size, a misaligned cache pointer) are reported by this one too; the
+    checks run before the scratch is cleared."""
+    import torch
+
+    B, Hq, Hkv, n, D = 1, 12, 4, 1000, 128  # Hq / Hkv = 3: no kernel for that group size
+    q = torch.zeros((B, Hq, D), dtype=torch.bfloat16, device=dev)
+    kv = torch.zeros((B, n, Hkv, D), dtype=torch.bfloat16, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    rc = jl.lib.jl_bifocal_decode_noalloc(_ptr(q), _ptr(kv), _ptr(kv), _ptr(out), _ptr(lse), B, Hq,
+                                          Hkv, n, n, D, 512, 64, 1e6, stream)
+    assert rc == jl.JL_ERR_UNSUPPORTED
+    mis = ctypes.c_void_p(kv.data_ptr() + 2)
+    rc = jl.lib.jl_bifocal_decode_noalloc(_ptr(q), mis, _ptr(kv), _ptr(out), _ptr(lse), B, 8, 4, n, n,
+                                          D, 512, 64, 1e6, stream)
+    assert rc == jl.JL_ERR_ALIGN

@@ -12,6 +12,8 @@ _BINDING_NAMES = (
     "jl_group_factor", "jl_rope_apply", "jl_version", "lib", "status_string",
     "jl_bifocal_decode_noalloc", "jl_debug_wait_timeout", "jl_bifocal_prefill_chunk",
     "jl_bifocal_decode_paged", "jl_bifocal_decode_paged_workspace_size", "jl_rope_cache_write",
+    "jl_group_factor_ex", "jl_bifocal_prefill_ex", "jl_bifocal_decode_ex", "JL_VARIANT_PER_QUERY_G",
+    "JL_VARIANT_SLIDING", "JL_VARIANT_QUERY_SHIFT", "JL_PREFILL_CTA_PAIR",
 )
 
 __all__ = list(_BINDING_NAMES)

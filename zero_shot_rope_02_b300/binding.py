@@ -32,8 +32,16 @@ EXPORTS = (
     "jl_bifocal_decode_workspace_size", "jl_bifocal_decode", "jl_debug_grouped_positions",
     "jl_debug_tile_classes", "jl_debug_status", "jl_bifocal_decode_noalloc",
     "jl_debug_wait_timeout", "jl_bifocal_prefill_chunk", "jl_bifocal_decode_paged",
-    "jl_bifocal_decode_paged_workspace_size", "jl_rope_cache_write",
+    "jl_bifocal_decode_paged_workspace_size", "jl_rope_cache_write", "jl_group_factor_ex",
+    "jl_bifocal_prefill_ex", "jl_bifocal_decode_ex",
 )
+
+# Variant flags of the _ex entry points (include/jetlong.h).
+JL_VARIANT_PER_QUERY_G = 1
+JL_VARIANT_SLIDING = 2
+JL_VARIANT_QUERY_SHIFT = 4
+# jl_bifocal_prefill_ex: the two-SM (cta_group::2) tile kernel where it applies
+JL_PREFILL_CTA_PAIR = 8
 
 
 class JetLongError(RuntimeError):
@@ -52,11 +60,16 @@ def _load() -> ctypes.CDLL:
         "jl_status_string": (ctypes.c_char_p, [i32]),
         "jl_version": (ctypes.c_char_p, []),
         "jl_group_factor": (i32, [i64, i64, ctypes.POINTER(ctypes.c_int32)]),
+        "jl_group_factor_ex": (i32, [i64, i64, i64, ctypes.c_uint, ctypes.POINTER(ctypes.c_int32)]),
         "jl_rope_apply": (i32, [p, i32, i32, i32, i32, i64, dbl, p]),
         "jl_rope_cache_write": (i32, [p, p, p, p, i32, i32, i32, i32, i32, i32, dbl, p]),
         "jl_bifocal_prefill": (i32, [p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, dbl, p]),
         "jl_bifocal_prefill_chunk": (i32, [p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                            dbl, p]),
+        "jl_bifocal_prefill_ex": (i32, [p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+                                        dbl, ctypes.c_uint, p]),
+        "jl_bifocal_decode_ex": (i32, [p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, i32, dbl,
+                                       ctypes.c_uint, p, sz, p]),
         "jl_bifocal_decode_workspace_size": (sz, [i32, i32, i32, i32, i32]),
         "jl_bifocal_decode": (i32, [p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, i32, dbl,
                                     p, sz, p]),
@@ -121,6 +134,15 @@ def jl_group_factor(s: int, L_pre: int) -> int:
     """g(s, L_pre) = max(1, ceil(s / L_pre)) from the library (host only)."""
     g = ctypes.c_int32(0)
     _check("jl_group_factor", lib.jl_group_factor(int(s), int(L_pre), ctypes.byref(g)))
+    return int(g.value)
+
+
+def jl_group_factor_ex(s: int, L_pre: int, w: int, flags: int) -> int:
+    """Group factor under variant flags (the query-shift rule with
+    JL_VARIANT_QUERY_SHIFT) from the library (host only)."""
+    g = ctypes.c_int32(0)
+    _check("jl_group_factor_ex", lib.jl_group_factor_ex(int(s), int(L_pre), int(w), int(flags),
+                                                        ctypes.byref(g)))
     return int(g.value)
 
 
@@ -201,6 +223,61 @@ def jl_bifocal_prefill_chunk(q, k_cache, v_cache, n_past: int, L_pre: int, w: in
            lib.jl_bifocal_prefill_chunk(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse), B,
                                         Hq, Hkv, S_new, int(n_past), n_cap, D, int(L_pre), int(w),
                                         float(theta), _stream(stream)))
+    return out, lse
+
+
+def jl_bifocal_prefill_ex(q, k_cache, v_cache, n_past: int, L_pre: int, w: int, theta: float, flags: int,
+                          out=None, lse=None, stream=None):
+    """Bifocal prefill with variant flags (JL_VARIANT_*) of S_new tokens at
+    positions n_past.. over the cache.  q [B,S_new,Hq,D]; caches [B,n_cap,Hkv,D]
+    bf16 (exact RoPE), rows 0..n_past+S_new-1 valid.  Returns (out, lse)."""
+    import torch
+
+    for t, nm in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, nm)
+    B, S_new, Hq, D = q.shape
+    _, n_cap, Hkv, Dk = k_cache.shape
+    if Dk != D or v_cache.shape != k_cache.shape or k_cache.shape[0] != B:
+        raise ValueError("caches must be [B, n_cap, Hkv, D] matching q")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, S_new), dtype=torch.float32, device=q.device)
+    _need(out, torch.bfloat16, "out")
+    _need(lse, torch.float32, "lse")
+    _check("jl_bifocal_prefill_ex",
+           lib.jl_bifocal_prefill_ex(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse), B, Hq, Hkv,
+                                     S_new, int(n_past), n_cap, D, int(L_pre), int(w), float(theta),
+                                     int(flags), _stream(stream)))
+    return out, lse
+
+
+def jl_bifocal_decode_ex(q, k_cache, v_cache, n: int, L_pre: int, w: int, theta: float, flags: int,
+                         workspace=None, out=None, lse=None, stream=None):
+    """jl_bifocal_decode with variant flags (JL_VARIANT_*).  Same arguments and
+    workspace as jl_bifocal_decode.  Returns (out bf16 [B,Hq,D], lse fp32 [B,Hq])."""
+    import torch
+
+    for t, nm in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, nm)
+    B, Hq, D = q.shape
+    _, n_cap, Hkv, Dk = k_cache.shape
+    if Dk != D or v_cache.shape != k_cache.shape or k_cache.shape[0] != B:
+        raise ValueError("caches must be [B, n_cap, Hkv, D] matching q")
+    if workspace is None:
+        nbytes = jl_bifocal_decode_workspace_size(B, Hq, Hkv, n, D)
+        workspace = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    _need(out, torch.bfloat16, "out")
+    _need(lse, torch.float32, "lse")
+    _check("jl_bifocal_decode_ex",
+           lib.jl_bifocal_decode_ex(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse), B, Hq, Hkv,
+                                    int(n), n_cap, D, int(L_pre), int(w), float(theta), int(flags),
+                                    _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                    _stream(stream)))
     return out, lse
 
 

@@ -69,8 +69,10 @@ static EncodeTiledFn encode_fn()
     return fn;
 }
 
-// A few recently encoded maps per host thread: repeated calls on the same
-// tensors (decode steps over one cache, benchmark loops) skip the encode.
+// Encoded maps per host thread, keyed by everything the encoding depends on:
+// repeated calls on the same tensors (a decode step's caches, one per layer;
+// benchmark loops) skip the driver's encode.  Open addressing on a hash of the
+// key; a full probe sequence evicts its first slot.
 namespace {
 struct MapKey {
     const void *base;
@@ -80,12 +82,19 @@ struct MapKey {
         return base == o.base && B == o.B && S == o.S && S_cap == o.S_cap && H == o.H && D == o.D &&
                box_d == o.box_d && box_rows == o.box_rows && sw == o.sw;
     }
+    uint64_t hash() const
+    {
+        uint64_t h = reinterpret_cast<uintptr_t>(base) * 0x9E3779B97F4A7C15ull;
+        const int f[8] = {B, S, S_cap, H, D, box_d, box_rows, sw};
+        for (int i = 0; i < 8; i++) h = (h ^ (uint64_t)(uint32_t)f[i]) * 0x100000001B3ull;
+        return h ^ (h >> 29);
+    }
 };
 struct MapCache {
-    static constexpr int N = 16;
+    static constexpr int N = 256, PROBE = 8;
     MapKey key[N];
     CUtensorMap map[N];
-    int used = 0, next = 0;
+    bool used[N] = {};
 };
 }  // namespace
 
@@ -97,16 +106,21 @@ bool make_bshd_map(CUtensorMap *m, const void *base, int B, int S, int S_cap, in
 {
     thread_local MapCache cache;
     const MapKey k{base, B, S, S_cap, H, D, box_d, box_rows, swizzle128 ? 1 : 0};
-    for (int i = 0; i < cache.used; i++)
-        if (cache.key[i] == k) {
+    const int h0 = (int)(k.hash() % MapCache::N);
+    int slot = -1;
+    for (int p = 0; p < MapCache::PROBE; p++) {
+        const int i = (h0 + p) % MapCache::N;
+        if (cache.used[i] && cache.key[i] == k) {
             *m = cache.map[i];
             return true;
         }
+        if (!cache.used[i] && slot < 0) slot = i;
+    }
     if (!encode_bshd_map(m, base, B, S, S_cap, H, D, box_d, box_rows, swizzle128)) return false;
-    cache.key[cache.next] = k;
-    cache.map[cache.next] = *m;
-    cache.next = (cache.next + 1) % MapCache::N;
-    if (cache.used < MapCache::N) cache.used++;
+    if (slot < 0) slot = h0;
+    cache.key[slot] = k;
+    cache.map[slot] = *m;
+    cache.used[slot] = true;
     return true;
 }
 
@@ -216,6 +230,23 @@ int jl_group_factor(int64_t s, int64_t L_pre, int32_t *g_out)
 {
     if (!g_out || s < 1 || L_pre < 1) return JL_ERR_ARG;
     int64_t g = jl::group_factor_host(s, L_pre);
+    if (g > INT32_MAX) return JL_ERR_OVERFLOW;
+    *g_out = (int32_t)g;
+    return JL_OK;
+}
+
+int jl_group_factor_ex(int64_t s, int64_t L_pre, int64_t w, unsigned flags, int32_t *g_out)
+{
+    if (!g_out || s < 1 || L_pre < 1 || w < 1) return JL_ERR_ARG;
+    if (flags & ~(unsigned)(JL_VARIANT_PER_QUERY_G | JL_VARIANT_SLIDING | JL_VARIANT_QUERY_SHIFT))
+        return JL_ERR_ARG;
+    if ((flags & JL_VARIANT_SLIDING) && flags != JL_VARIANT_SLIDING) return JL_ERR_ARG;
+    int64_t g = jl::group_factor_host(s, L_pre);
+    if (flags & JL_VARIANT_SLIDING) g = 1;
+    if (flags & JL_VARIANT_QUERY_SHIFT) {
+        g = jl::group_factor_shift_host(s, L_pre, w);
+        if (g < 1) return JL_ERR_ARG;
+    }
     if (g > INT32_MAX) return JL_ERR_OVERFLOW;
     *g_out = (int32_t)g;
     return JL_OK;

@@ -61,12 +61,13 @@ struct DecodeArgs {
     float *part_o;           // [B, Hq, splits, D]
     int *status;
     int Hq, Hkv, n, w, g, splits, chunk;
+    int qshift;              // added to the query's correction offset (query-shift variant)
     float scale_log2;        // tau * log2(e)
     // paged variant: per-sequence lengths and the page table (device), the
     // pages' row count, table width and the pretrained window (g per sequence)
     const int *seq_lens;     // [B]
     const int *block_table;  // [B, max_pages]
-    int page_size, max_pages, L;
+    int page_size, max_pages, num_pages, L;
 };
 
 // Named barrier over the compute warps only (the producer warp never joins).
@@ -168,9 +169,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int row = j_begin + blk * kKB;
                 int r_in = row, unit = b;
                 if constexpr (PAGED) {
-                    // a page id outside the pool reads zeros (TMA bounds), never faults
+                    // a page id outside the pool reads zeros (TMA bounds), never
+                    // faults, and is reported: those keys would score 0 with V = 0
                     unit = a.block_table[(size_t)b * a.max_pages + row / a.page_size];
                     r_in = row % a.page_size;
+                    if ((unsigned)unit >= (unsigned)a.num_pages) jl::record_status(a.status, JL_ERR_GUARD);
                 }
                 tma_load_4d(sbase + C::OFF_K + s * C::BLOCK_BYTES, &tk, full(s), 0, hk, r_in, unit);
                 tma_load_4d(sbase + C::OFF_V + s * C::BLOCK_BYTES, &tv, full(s), 0, hk, r_in, unit);
@@ -193,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     compute_sync();
     if (g > 1) {
-        const int di = jl::delta_pos(n - 1, g);
+        const int di = jl::delta_pos(n - 1, g) + a.qshift;
         for (int d = tid; d < HALF; d += kCompute) {
             float sn, cs;
             jl::phase_sincos(di, pt.f[d], &sn, &cs);
@@ -355,6 +358,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
             if (lane == 0) {
+                // an infinite or NaN score (an input or corrected key out of range)
+                if (!(sum < INFINITY)) jl::record_status(a.status, JL_ERR_GUARD);
                 const float fac = (m_old == -INFINITY) ? 0.f : exp2f(m_old - off);
                 st_l[h] = st_l[h] * fac + sum;
                 st_m[h] = m_new;
@@ -464,33 +469,56 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     }
     compute_sync();
-    for (int t = tid; t < GRP * D; t += kCompute) {
-        const int h = t / D, d = t % D;
+    // each thread: 4 consecutive dims of one head, 8 splits' loads in flight
+    for (int t = tid; t < GRP * D / 4; t += kCompute) {
+        const int h = (4 * t) / D, d = (4 * t) % D;
         const float *po = a.part_o + (hq0 + h) * a.splits * D + d;
-        float o0 = 0.f, o1 = 0.f;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
         int q = 0;
-        for (; q + 1 < a.splits; q += 2) {
-            o0 = fmaf(mw[h * 256 + q], __ldcg(po + (size_t)q * D), o0);
-            o1 = fmaf(mw[h * 256 + q + 1], __ldcg(po + (size_t)(q + 1) * D), o1);
+        for (; q + 8 <= a.splits; q += 8) {
+            float4 x[8];
+#pragma unroll
+            for (int u = 0; u < 8; u++) x[u] = __ldcg(reinterpret_cast<const float4 *>(po + (size_t)(q + u) * D));
+#pragma unroll
+            for (int u = 0; u < 8; u++) {
+                const float wgt = mw[h * 256 + q + u];
+                o.x = fmaf(wgt, x[u].x, o.x);
+                o.y = fmaf(wgt, x[u].y, o.y);
+                o.z = fmaf(wgt, x[u].z, o.z);
+                o.w = fmaf(wgt, x[u].w, o.w);
+            }
         }
-        if (q < a.splits) o0 = fmaf(mw[h * 256 + q], __ldcg(po + (size_t)q * D), o0);
-        a.out[(hq0 + h) * D + d] = __float2bfloat16_rn((o0 + o1) / st_l[h]);
+        for (; q < a.splits; q++) {
+            const float4 x = __ldcg(reinterpret_cast<const float4 *>(po + (size_t)q * D));
+            const float wgt = mw[h * 256 + q];
+            o.x = fmaf(wgt, x.x, o.x);
+            o.y = fmaf(wgt, x.y, o.y);
+            o.z = fmaf(wgt, x.z, o.z);
+            o.w = fmaf(wgt, x.w, o.w);
+        }
+        const float inv = 1.f / st_l[h];
+        __nv_bfloat16 *dst = a.out + (hq0 + h) * D + d;
+        *reinterpret_cast<uint2 *>(dst) = make_uint2(jl::pack_bf16x2(o.x * inv, o.y * inv),
+                                                     jl::pack_bf16x2(o.z * inv, o.w * inv));
     }
     if (tid < GRP) a.lse[hq0 + tid] = (st_m[tid] + log2f(st_l[tid])) * kLn2;
     if (tid == 0) a.counters[b * a.Hkv + hk] = 0;  // ready for the next call
 }
 
-// Split plan: two CTAs per SM (shared memory and registers allow two), at
-// most 256 splits per (batch, kv head), chunks a multiple of the 64-key block.
-// splits_cap bounds splits for every n, and the workspace is sized by it, so
-// one workspace serves every cache length for the same (B, Hq, Hkv, D).
+// Split plan: as many CTAs as the kernel keeps resident (two per SM: shared
+// memory and registers allow two), at most 256 splits per (batch, kv head),
+// chunks a multiple of the 64-key block.  splits_cap bounds splits for every
+// n, and the workspace is sized by it, so one workspace serves every cache
+// length for the same (B, Hq, Hkv, D).
 struct Plan {
     int splits, chunk, splits_cap;
 };
 
-Plan make_plan(int B, int Hkv, int n)
+int resident_ctas(int) { return 2; }
+
+Plan make_plan(int B, int Hkv, int grp, int n)
 {
-    const long long target_ctas = 148 * 2;
+    const long long target_ctas = 148LL * resident_ctas(grp);
     long long per_head = (target_ctas + (long long)B * Hkv - 1) / ((long long)B * Hkv);
     if (per_head < 1) per_head = 1;
     if (per_head > 256) per_head = 256;
@@ -501,11 +529,11 @@ Plan make_plan(int B, int Hkv, int n)
 }
 
 // Paged batches mix lengths, so the split count is sized for the longest
-// sequence as if it alone filled the GPU (two CTAs per SM over its kv heads);
-// the splits of shorter sequences past their end exit at once.
-Plan make_paged_plan(int Hkv, int max_n)
+// sequence as if it alone filled the GPU (every resident CTA over its kv
+// heads); the splits of shorter sequences past their end exit at once.
+Plan make_paged_plan(int Hkv, int grp, int max_n)
 {
-    long long per_head = (148LL * 2 + Hkv - 1) / Hkv;
+    long long per_head = (148LL * resident_ctas(grp) + Hkv - 1) / Hkv;
     if (per_head > 256) per_head = 256;
     long long chunk = (max_n + per_head - 1) / per_head;
     chunk = (chunk + kKB - 1) / kKB * kKB;
@@ -597,6 +625,27 @@ int dispatch(int D, int grp, const DecodeArgs &a, int B, const CUtensorMap &tk, 
     }
 }
 
+// Every argument check of the contiguous-cache decode that does not depend on
+// the workspace: run before anything is enqueued, by both entry points that
+// take that cache.
+int decode_args_status(const void *q, const void *k_cache, const void *v_cache, const void *out,
+                       const float *lse, int B, int Hq, int Hkv, int n, int n_cap, int D, int L_pre,
+                       int w, double theta)
+{
+    if (!q || !k_cache || !v_cache || !out || !lse) return JL_ERR_ARG;
+    if (B < 1 || Hq < 1 || Hkv < 1 || n < 1 || n_cap < n || L_pre < 1 || w < 1 || !(theta > 0.0) ||
+        Hq % Hkv != 0)
+        return JL_ERR_ARG;
+    if (D != 64 && D != 128) return JL_ERR_UNSUPPORTED;
+    const int grp = Hq / Hkv;
+    if (grp != 1 && grp != 2 && grp != 4 && grp != 8) return JL_ERR_UNSUPPORTED;
+    if (!jl::aligned16(q) || !jl::aligned16(out) || !jl::aligned16(lse) || !jl::aligned16(k_cache) ||
+        !jl::aligned16(v_cache))
+        return JL_ERR_ALIGN;
+    if ((long long)B * n_cap * Hkv * D > ((long long)1 << 46)) return JL_ERR_OVERFLOW;
+    return JL_OK;
+}
+
 // The argument checks and workspace layout both entry points share; fills the
 // length-independent fields of `a`.
 int common_setup(DecodeArgs &a, const void *q, void *out, float *lse, int B, int Hq, int Hkv, int n,
@@ -609,7 +658,7 @@ int common_setup(DecodeArgs &a, const void *q, void *out, float *lse, int B, int
     const int grp = Hq / Hkv;
     if (grp != 1 && grp != 2 && grp != 4 && grp != 8) return JL_ERR_UNSUPPORTED;
     if (!jl::aligned16(q) || !jl::aligned16(out) || !jl::aligned16(lse)) return JL_ERR_ALIGN;
-    Plan p = paged ? make_paged_plan(Hkv, n) : make_plan(B, Hkv, n);
+    Plan p = paged ? make_paged_plan(Hkv, grp, n) : make_plan(B, Hkv, grp, n);
     size_t off_ml = 0, off_o = 0;
     size_t need = ws_layout(B, Hq, Hkv, D, p, &off_ml, &off_o);
     if (!workspace || ws_bytes < need) return JL_ERR_WORKSPACE;
@@ -639,29 +688,27 @@ int common_setup(DecodeArgs &a, const void *q, void *out, float *lse, int B, int
 extern "C" size_t jl_bifocal_decode_workspace_size(int B, int Hq, int Hkv, int n, int D)
 {
     if (!shapes_ok(B, Hq, Hkv, n, D)) return 0;
-    Plan p = make_plan(B, Hkv, n);
+    Plan p = make_plan(B, Hkv, Hq / Hkv, n);
     return ws_layout(B, Hq, Hkv, D, p, nullptr, nullptr);
 }
 
 extern "C" size_t jl_bifocal_decode_paged_workspace_size(int B, int Hq, int Hkv, int max_n, int D)
 {
     if (!shapes_ok(B, Hq, Hkv, max_n, D)) return 0;
-    return ws_layout(B, Hq, Hkv, D, make_paged_plan(Hkv, max_n), nullptr, nullptr);
+    return ws_layout(B, Hq, Hkv, D, make_paged_plan(Hkv, Hq / Hkv, max_n), nullptr, nullptr);
 }
 
-extern "C" int jl_bifocal_decode(const void *q, const void *k_cache, const void *v_cache, void *out,
-                                 float *lse, int B, int Hq, int Hkv, int n, int n_cap, int D,
-                                 int L_pre, int w, double theta, void *workspace, size_t ws_bytes,
-                                 void *stream)
+// The contiguous-cache decode with group factor g and the query's correction
+// offset shifted by qshift (arguments already checked by decode_args_status).
+static int decode_impl(const void *q, const void *k_cache, const void *v_cache, void *out, float *lse,
+                       int B, int Hq, int Hkv, int n, int n_cap, int D, int L_pre, int w, double theta,
+                       int g, int qshift, void *workspace, size_t ws_bytes, void *stream)
 {
-    if (!k_cache || !v_cache) return JL_ERR_ARG;
-    if (n_cap < n) return JL_ERR_ARG;
     DecodeArgs a;
     int rc = common_setup(a, q, out, lse, B, Hq, Hkv, n, D, L_pre, w, theta, workspace, ws_bytes, false);
     if (rc != JL_OK) return rc;
-    if (!jl::aligned16(k_cache) || !jl::aligned16(v_cache)) return JL_ERR_ALIGN;
-    if ((long long)B * n_cap * Hkv * D > ((long long)1 << 46)) return JL_ERR_OVERFLOW;
-    a.g = (int)jl::group_factor_host(n, L_pre);
+    a.g = g;
+    a.qshift = qshift;
     const jl::PhaseTable *pt = nullptr;
     const DecRot *rot = nullptr;
     if (!host_tables(D, theta, a.g, &pt, &rot)) return JL_ERR_ARG;
@@ -672,6 +719,49 @@ extern "C" int jl_bifocal_decode(const void *q, const void *k_cache, const void 
         !jl::make_bshd_map(&tv, v_cache, B, n, n_cap, Hkv, D, D, kKB, false))
         return JL_ERR_CUDA;
     return dispatch<false>(D, Hq / Hkv, a, B, tk, tv, *pt, *rot, (cudaStream_t)stream);
+}
+
+extern "C" int jl_bifocal_decode(const void *q, const void *k_cache, const void *v_cache, void *out,
+                                 float *lse, int B, int Hq, int Hkv, int n, int n_cap, int D,
+                                 int L_pre, int w, double theta, void *workspace, size_t ws_bytes,
+                                 void *stream)
+{
+    const int rc = decode_args_status(q, k_cache, v_cache, out, lse, B, Hq, Hkv, n, n_cap, D, L_pre, w,
+                                      theta);
+    if (rc != JL_OK) return rc;
+    return decode_impl(q, k_cache, v_cache, out, lse, B, Hq, Hkv, n, n_cap, D, L_pre, w, theta,
+                       (int)jl::group_factor_host(n, L_pre), 0, workspace, ws_bytes, stream);
+}
+
+extern "C" int jl_bifocal_decode_ex(const void *q, const void *k_cache, const void *v_cache, void *out,
+                                    float *lse, int B, int Hq, int Hkv, int n, int n_cap, int D, int L_pre,
+                                    int w, double theta, unsigned flags, void *workspace, size_t ws_bytes,
+                                    void *stream)
+{
+    int rc = decode_args_status(q, k_cache, v_cache, out, lse, B, Hq, Hkv, n, n_cap, D, L_pre, w, theta);
+    if (rc != JL_OK) return rc;
+    if (flags & ~(unsigned)(JL_VARIANT_PER_QUERY_G | JL_VARIANT_SLIDING | JL_VARIANT_QUERY_SHIFT))
+        return JL_ERR_ARG;
+    if ((flags & JL_VARIANT_SLIDING) && flags != JL_VARIANT_SLIDING) return JL_ERR_ARG;
+    if (flags & JL_VARIANT_SLIDING) {
+        // only the last min(n, w) keys are attended, all exact: the plain decode
+        // over the cache rows from n - w on (g = 1; positions play no part in
+        // exact scores of exact-RoPE vectors).  The view keeps the cache's batch
+        // stride of n_cap rows; its last batch entry ends at row n <= n_cap.
+        const int n_in = n < w ? n : w;
+        const size_t skip = (size_t)(n - n_in) * Hkv * D * sizeof(__nv_bfloat16);
+        return decode_impl(q, (const char *)k_cache + skip, (const char *)v_cache + skip, out, lse, B, Hq,
+                           Hkv, n_in, n_cap, D, n_in, w, theta, 1, 0, workspace, ws_bytes, stream);
+    }
+    if (flags & JL_VARIANT_QUERY_SHIFT) {
+        const long long g = jl::group_factor_shift_host(n, L_pre, w);
+        if (g < 1) return JL_ERR_ARG;
+        return decode_impl(q, k_cache, v_cache, out, lse, B, Hq, Hkv, n, n_cap, D, L_pre, w, theta, (int)g,
+                           (int)(w - w / g), workspace, ws_bytes, stream);
+    }
+    // per-query g: the single query at n - 1 has the call's length n
+    return decode_impl(q, k_cache, v_cache, out, lse, B, Hq, Hkv, n, n_cap, D, L_pre, w, theta,
+                       (int)jl::group_factor_host(n, L_pre), 0, workspace, ws_bytes, stream);
 }
 
 extern "C" int jl_bifocal_decode_paged(const void *q, const void *k_pages, const void *v_pages,
@@ -695,6 +785,7 @@ extern "C" int jl_bifocal_decode_paged(const void *q, const void *k_pages, const
     a.block_table = block_table;
     a.page_size = page_size;
     a.max_pages = max_pages;
+    a.num_pages = num_pages;
     const jl::PhaseTable *pt = nullptr;
     const DecRot *rot = nullptr;
     if (!host_tables(D, theta, 1, &pt, &rot)) return JL_ERR_ARG;  // per-sequence g on the device
@@ -752,12 +843,11 @@ extern "C" int jl_bifocal_decode_noalloc(const void *q, const void *k_cache, con
                                          int n_cap, int D, int L_pre, int w, double theta,
                                          void *stream)
 {
-    if (!q || !k_cache || !v_cache || !out || !lse) return JL_ERR_ARG;
-    if (B < 1 || Hq < 1 || Hkv < 1 || n < 1 || n_cap < n || L_pre < 1 || w < 1 ||
-        !(theta > 0.0) || Hq % Hkv != 0)
-        return JL_ERR_ARG;
-    if (D != 64 && D != 128) return JL_ERR_UNSUPPORTED;
-    const Plan p = make_plan(B, Hkv, n);
+    // every check runs before the scratch is touched: a rejected call enqueues nothing
+    const int rc = decode_args_status(q, k_cache, v_cache, out, lse, B, Hq, Hkv, n, n_cap, D, L_pre, w,
+                                      theta);
+    if (rc != JL_OK) return rc;
+    const Plan p = make_plan(B, Hkv, Hq / Hkv, n);
     size_t off_ml = 0, off_o = 0;
     const size_t need = ws_layout(B, Hq, Hkv, D, p, &off_ml, &off_o);
     if (need > kNoAllocScratchBytes) return JL_ERR_WORKSPACE;  // beyond the fixed scratch

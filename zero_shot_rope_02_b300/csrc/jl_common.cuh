@@ -46,6 +46,20 @@ void rotation_host(const PhaseTable &t, int d, long long offset, float *c, float
 // floor((s-1)/g) <= L-1 (ResearchPod summary: smallest integer grouping).
 inline int64_t group_factor_host(int64_t s, int64_t L) { return s <= L ? 1 : (s + L - 1) / L; }
 
+// Host: group factor of the query-shift variant -- the smallest g >= 1 with
+// floor((s-1)/g) + w - floor(w/g) <= L-1, the largest aliased distance once the
+// aliased query position is shifted by w - floor(w/g) (Self-Extend's grouping,
+// named as a baseline in the ResearchPod summary).  -1 when no g does (w >= L
+// while s > L).  Smaller g than the unshifted factor cannot work (the shift is
+// >= 0), and g = max(s, w) + 1 always does once w < L, so the search ends.
+inline int64_t group_factor_shift_host(int64_t s, int64_t L, int64_t w)
+{
+    if (s <= L) return 1;
+    if (w >= L) return -1;
+    for (int64_t g = (s + L - 1) / L;; g++)
+        if ((s - 1) / g + (w - w / g) <= L - 1) return g;
+}
+
 // Host: pointer to the device status word of the current device (cached per
 // device).  Returns nullptr if CUDA is unusable.
 int *status_word_ptr();

@@ -82,12 +82,16 @@ struct Cfg {
 };
 
 struct Params {
-    __nv_bfloat16 *out;  // [B, Sq, Hq, D]
-    float *lse;          // [B, Hq, Sq]
+    __nv_bfloat16 *out;  // row 0 of this launch's rows; batch stride q_rows rows
+    float *lse;          // column 0 of this launch's rows; row stride lse_stride
     int *status;
     // S: keys (positions 0..S-1, the length that sets g); the Sq query rows sit
     // at positions pos0..pos0+Sq-1 = S-Sq..S-1 (pos0 = 0, Sq = S: full prefill)
     int B, Hq, Hkv, S, Sq, pos0, w, g, grp, n_qtiles, pairs;  // pairs = grp / NH
+    int q_rows;          // rows per batch entry of q / out (>= Sq)
+    int lse_stride;      // elements between (b, h) rows of lse (>= Sq)
+    int qshift;          // added to the query's correction offset (query-shift variant)
+    int sliding;         // sliding-window layer: keys with i - j >= w are not attended
     float scale_log2;    // tau * log2(e)
 };
 
@@ -137,13 +141,16 @@ struct RotConsts {
 // remote K tiles come in order 0, 1, 2, ..., so the chains carry over and
 // are re-anchored from the exact phase only every kReanchorTiles tiles.
 // Otherwise every tile is anchored exactly and each step picks a or b.
-template <int D>
+//
+// ROWS = 64 serves the pair kernel, whose CTAs hold one half of each K tile:
+// its chains then skip the other CTA's 64 rows after every tile.
+template <int D, int ROWS = 128>
 struct Corrector {
-    static constexpr int CPR = D / 16;       // chunk pairs per row
-    static constexpr int RPS = 128 / CPR;    // rows per step
-    static constexpr int STEPS = 128 / RPS;  // rows per thread
+    static constexpr int CPR = D / 16;        // chunk pairs per row
+    static constexpr int RPS = 128 / CPR;     // rows per step
+    static constexpr int STEPS = ROWS / RPS;  // rows per thread
     static constexpr int kReanchorTiles = 32;
-    static constexpr uint32_t REGION = kBM * 64 * 2;
+    static constexpr uint32_t REGION = ROWS * 64 * 2;  // one 64-column box of the tile
     int c, n0, g, next_kt;
     bool uni;
     const unsigned long long *F;  // this thread's 8 phases (parameter space)
@@ -226,11 +233,11 @@ struct Corrector {
         }
     }
 
-    // exact anchors of both chains at rows p and p + RPS
-    __device__ void anchor(int p)
+    // exact anchors of both chains at rows p and p + RPS (offsets delta + off)
+    __device__ void anchor(int p, int off = 0)
     {
-        sincos8(jl::delta_pos(p, g), ec, es);
-        sincos8(jl::delta_pos(p + RPS, g), oc, os);
+        sincos8(jl::delta_pos(p, g) + off, ec, es);
+        sincos8(jl::delta_pos(p + RPS, g) + off, oc, os);
     }
 
     // g divides RPS: rows n0 + 2k*RPS on the even chain, n0 + (2k+1)*RPS on
@@ -267,11 +274,11 @@ struct Corrector {
     }
 
     // any g: exact anchor at row n0, then per RPS rows a or b
-    __device__ void run_generic(uint32_t tile, int p0) const
+    __device__ void run_generic(uint32_t tile, int p0, int off = 0) const
     {
         jl::f32x2 zc[4], zs[4];
         const int p = p0 + n0;
-        sincos8(jl::delta_pos(p, g), zc, zs);
+        sincos8(jl::delta_pos(p, g) + off, zc, zs);
         const int rs = RPS % g;
         int jm = p % g;
 #pragma unroll 1
@@ -299,27 +306,45 @@ struct Corrector {
         }
     }
 
-    // the query tile at rows p0..p0+127 (leaves the K chains to be re-anchored)
-    __device__ void run_q(uint32_t tile, int p0)
+    // the query tile at rows p0..p0+127, offsets delta + qshift (leaves the K
+    // chains to be re-anchored)
+    __device__ void run_q(uint32_t tile, int p0, int qshift)
     {
         if (uni) {
-            anchor(p0 + n0);
+            anchor(p0 + n0, qshift);
             run_uni(tile);
             next_kt = -1;
         } else {
-            run_generic(tile, p0);
+            run_generic(tile, p0, qshift);
         }
     }
 
-    // remote K tile kt (tiles arrive in increasing order)
-    __device__ void run_k(uint32_t tile, int kt)
+    // remote K tile kt (tiles arrive in increasing order); row0 = position of
+    // the held rows' first row within the 128-key tile (0, or 64 for the
+    // second half in the pair kernel)
+    __device__ void run_k(uint32_t tile, int kt, int row0 = 0)
     {
         if (uni) {
-            if (kt != next_kt || kt % kReanchorTiles == 0) anchor(kt * kBN + n0);
+            if (kt != next_kt || kt % kReanchorTiles == 0) anchor(kt * kBN + row0 + n0);
             run_uni(tile);
+            if (ROWS < kBN) {
+                // skip the rows the other CTA holds: the chains step 2 RPS rows per a2
+                jl::f32x2 rcs[4], rsn[4], rns[4];
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    rcs[q] = ld2(rc->a2c + 8 * c + 2 * q);
+                    rsn[q] = ld2(rc->a2s + 8 * c + 2 * q);
+                    rns[q] = ld2(rc->a2ns + 8 * c + 2 * q);
+                }
+#pragma unroll 1
+                for (int k = 0; k < (kBN - ROWS) / (2 * RPS); k++) {
+                    cmul(ec, es, rcs, rsn, rns);
+                    cmul(oc, os, rcs, rsn, rns);
+                }
+            }
             next_kt = kt + 1;
         } else {
-            run_generic(tile, kt * kBN);
+            run_generic(tile, kt * kBN + row0);
         }
     }
 };
@@ -390,8 +415,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q_row0 = qt * kBM;   // first row of the tile in q / out / lse
     const int i0 = p.pos0 + q_row0;  // its position
     const int S = p.S, w = p.w, g = p.g;
+    // tiles are classified against the window as for any g > 1 when the layer
+    // is a sliding window (g itself plays no part there)
+    const int g_cls = p.sliding ? 2 : g;
     Visit vis;
-    vis.init(i0, (min(i0 + kBM, S) - 1) / kBN, S, w, g);
+    vis.init(i0, (min(i0 + kBM, S) - 1) / kBN, S, w, g_cls);
+    if (p.sliding) {
+        // nothing outside the window is attended: no remote phase
+        vis.T -= vis.nr;
+        vis.nr = 0;
+    }
     const int T = vis.T, NR = vis.nr;
 
     if (threadIdx.x == 0) {
@@ -566,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int kt = vis.kt(v);
                 const bool remote = vis.remote(v);
                 const int j0 = kt * kBN;
-                const bool band = jl::tile_class(i0, j0, kBM, kBN, S, w, g) == jl::kTileBand;
+                const bool band = jl::tile_class(i0, j0, kBM, kBN, S, w, g_cls) == jl::kTileBand;
                 const bool masked = band || (j0 + kBN - 1 > i0) || (j0 + kBN > S);
                 // load 64 score columns (half hh) as raw fp32 bits with both TMEM
                 // loads in flight; keys that are in the future, past the end, or
@@ -688,9 +721,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok) ok = wait_bar_warp(bar(C::B_ODONE + n), (T - 1) & 1, wc);
             if (ok) {
                 tc_fence_after();
+                // a row sum that is not finite comes from an infinite or NaN score
+                // (an input or corrected operand out of range): report it
+                if (!(l < INFINITY)) jl::record_status(p.status, JL_ERR_GUARD);
                 const float inv_l = 1.f / l;
                 const int il = i - p.pos0;  // row in out / lse (valid while i < S)
-                __nv_bfloat16 *orow = p.out + (((size_t)b * p.Sq + il) * p.Hq + h) * D;
+                __nv_bfloat16 *orow = p.out + (((size_t)b * p.q_rows + il) * p.Hq + h) * D;
 #pragma unroll 1
                 for (int ch = 0; ch < D / 32; ch++) {
                     uint32_t o[32];
@@ -708,7 +744,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
                     }
                 }
-                if (i < S) p.lse[((size_t)b * p.Hq + h) * p.Sq + il] = (m_used + log2f(l)) * kLn2;
+                if (i < S) p.lse[((size_t)b * p.Hq + h) * p.lse_stride + il] = (m_used + log2f(l)) * kLn2;
             }
         }
     } else {
@@ -725,7 +761,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = wait_bar_warp(bar(C::B_QFULL), 0, wc);
         if (ok && NR > 0) {
 #pragma unroll 1
-            for (int n = 0; n < NH; n++) cor.run_q(sQ + n * C::TILE, i0);
+            for (int n = 0; n < NH; n++) cor.run_q(sQ + n * C::TILE, i0, p.qshift);
         }
         for (int u = 0; ok && u <= T; u++) {
             if (u < T) {
@@ -753,6 +789,548 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 13) tmem_dealloc(tmem, 512);
 }
 
+// ---------------------------------------------------------------- pair kernel
+// The same computation with two SMs per tile (cta_group::2 MMAs, M = 256): a
+// cluster of two CTAs covers one 128-row query tile of FOUR heads that share a
+// kv head, two heads per CTA.  Each CTA loads -- and on remote tiles corrects
+// -- one half of every K tile (64 keys), and loads one half of every V tile
+// (64 of the 128 dims), so per SM the correction work and the K / V
+// shared-memory traffic are half those of the single-CTA kernel while every
+// corrected key still serves 4 x 128 query rows.  One thread of the even CTA
+// issues the MMAs of both (A rows from each CTA's own Q or P, B split along N
+// between the CTAs, D in each CTA's own TMEM) and multicasts every commit to
+// both CTAs' barriers; warps of either CTA arrive on the even CTA's barriers
+// through the cluster window.  Roles, virtual tiles and barrier phases are
+// those of prefill_kernel; arrivals on the even CTA's barriers come one per
+// warp.
+struct PairCfg {
+    static constexpr int D = 128;
+    static constexpr int QTILE = kBM * D * 2;   // one head's 128 query rows: 32 KB
+    static constexpr int QREG = kBM * 128;      // one 64-column box of it: 16 KB
+    static constexpr int KHALF = 64 * D * 2;    // 64 keys x 128 dims: 16 KB
+    static constexpr int KREG = 64 * 128;       // one 64-column box of it: 8 KB
+    static constexpr int VHALF = kBN * 64 * 2;  // 128 keys x 64 dims: 16 KB
+    static constexpr int NK = 4, NV = 4;
+    static_assert(NV <= NK, "V ring deeper than the K ring");
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = OFF_Q + 2 * QTILE;
+    static constexpr int OFF_V = OFF_K + NK * KHALF;
+    static constexpr int OFF_BAR = OFF_V + NV * VHALF;
+    static constexpr int SMEM = OFF_BAR + 512 + 1024;  // + alignment slack
+    static constexpr int B_QFULL = 0, B_K0READY = 1, B_QFREE = 2, B_DRAIN = 3, B_KFULL = 4,
+                         B_KEMPTY = B_KFULL + NK, B_GO = B_KEMPTY + NK, B_VFULL = B_GO + NK,
+                         B_VEMPTY = B_VFULL + NV, B_SFULL = B_VEMPTY + NV, B_PFULL = B_SFULL + 2,
+                         B_ODONE = B_PFULL + 2, NBAR = B_ODONE + 2;
+    static constexpr int OFF_TMEM_SLOT = 448, OFF_ABORT = 452;
+    static_assert(NBAR * 8 <= OFF_TMEM_SLOT, "barrier area");
+    static_assert(SMEM <= 232448, "shared memory budget");
+    // arrivals on the even CTA's barriers: one per warp of both CTAs
+    static constexpr uint32_t K0_COUNT = 2 * 4;           // correction warps
+    static constexpr uint32_t GO_COUNT = 2 * (4 + 4 + 1);  // head-0 softmax, correction, V producer
+    static constexpr uint32_t P1_COUNT = 2 * 4;           // head-1 softmax
+    static constexpr uint16_t BOTH = 0x3;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                        const __grid_constant__ CUtensorMap tv, const Params p,
+                        const __grid_constant__ jl::PhaseTable pt, const __grid_constant__ RotConsts rc)
+{
+    using C = PairCfg;
+    constexpr int D = C::D, NK = C::NK, NV = C::NV;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~(uintptr_t)1023);
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sQ = sbase + C::OFF_Q, sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
+    const uint32_t bar0 = sbase + C::OFF_BAR;
+    auto bar = [&](int idx) -> uint32_t { return bar0 + 8u * (uint32_t)idx; };
+    // the even CTA's copy of a barrier, in the cluster window
+    auto lead = [&](int idx) -> uint32_t { return mapa_shared(bar(idx), 0); };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_BAR + C::OFF_TMEM_SLOT);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_BAR + C::OFF_ABORT);
+    const WaitCtx wc{p.status, abort_flag};
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();  // = blockIdx.x & 1
+    // blockIdx.x >> 1 walks (query tile, quad of heads), quad fastest, longest
+    // rows first; the rank picks the head pair of the quad
+    const int quads = p.pairs / 2;
+    const int cl = (int)blockIdx.x >> 1;
+    const int qt = p.n_qtiles - 1 - cl / quads;
+    const int hk = (int)blockIdx.y % p.Hkv;
+    const int b = (int)blockIdx.y / p.Hkv;
+    const int h0 = hk * p.grp + (2 * (cl % quads) + (int)rank) * 2;
+    const int q_row0 = qt * kBM;
+    const int i0 = p.pos0 + q_row0;
+    const int S = p.S, w = p.w, g = p.g;
+    const int g_cls = p.sliding ? 2 : g;
+    Visit vis;
+    vis.init(i0, (min(i0 + kBM, S) - 1) / kBN, S, w, g_cls);
+    if (p.sliding) {
+        vis.T -= vis.nr;
+        vis.nr = 0;
+    }
+    const int T = vis.T, NR = vis.nr;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(C::B_QFULL), 1);
+        mbar_init(bar(C::B_K0READY), C::K0_COUNT);
+        mbar_init(bar(C::B_QFREE), 1);
+        mbar_init(bar(C::B_DRAIN), 1);
+        for (int s = 0; s < NK; s++) {
+            mbar_init(bar(C::B_KFULL + s), 1);
+            mbar_init(bar(C::B_KEMPTY + s), 1);
+            mbar_init(bar(C::B_GO + s), C::GO_COUNT);
+        }
+        for (int s = 0; s < NV; s++) {
+            mbar_init(bar(C::B_VFULL + s), 1);
+            mbar_init(bar(C::B_VEMPTY + s), 1);
+        }
+        for (int n = 0; n < 2; n++) {
+            mbar_init(bar(C::B_SFULL + n), 1);
+            mbar_init(bar(C::B_PFULL + n), C::P1_COUNT);
+            mbar_init(bar(C::B_ODONE + n), 1);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 13) {
+        tmem_alloc2(smem_u32(tmem_slot), 512);
+        tmem_relinquish2();
+    }
+    // both CTAs' barriers and TMEM exist before anyone arrives or issues
+    __syncwarp();
+    tc_fence_before();
+    cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 12) {
+        // ------------------------------------------------------------ producer: Q and K halves
+        if (lane == 0) {
+            prefetch_tmap(&tq);
+            prefetch_tmap(&tk);
+            auto load_q = [&]() {
+                mbar_arrive_expect_tx(bar(C::B_QFULL), 2 * C::QTILE);
+#pragma unroll
+                for (int n = 0; n < 2; n++)
+#pragma unroll
+                    for (int r = 0; r < 2; r++)
+                        tma_load_4d(sQ + n * C::QTILE + r * C::QREG, &tq, bar(C::B_QFULL), r * 64, h0 + n,
+                                    q_row0, b);
+            };
+            load_q();
+            int issued = 0;
+            bool ok = true;
+            for (int v = 0; v < T; v++) {
+                if (v == NR && NR > 0) {
+                    if (!(ok = wait_bar_cl(bar(C::B_QFREE), 0, wc))) break;
+                    load_q();
+                }
+                const int sk = v % NK;
+                if (!(ok = wait_bar_cl(bar(C::B_KEMPTY + sk), ((v / NK) & 1) ^ 1, wc))) break;
+                mbar_arrive_expect_tx(bar(C::B_KFULL + sk), C::KHALF);
+#pragma unroll
+                for (int r = 0; r < 2; r++)
+                    tma_load_4d(sK + sk * C::KHALF + r * C::KREG, &tk, bar(C::B_KFULL + sk), r * 64, hk,
+                                vis.kt(v) * kBN + 64 * (int)rank, b);
+                issued = v + 1;
+            }
+            if (!ok) {
+                for (int v = issued - NK < 0 ? 0 : issued - NK; v < issued; v++)
+                    drain_bar(bar(C::B_KFULL + v % NK), (v / NK) & 1);
+            }
+        }
+    } else if (warp == 14) {
+        // ------------------------------------------------------------ producer: V halves
+        if (lane == 0) {
+            prefetch_tmap(&tv);
+            int issued = 0;
+            bool ok = true;
+            for (int v = 0; v < T; v++) {
+                const int sv = v % NV;
+                if (!(ok = wait_bar_cl(bar(C::B_VEMPTY + sv), ((v / NV) & 1) ^ 1, wc))) break;
+                mbar_arrive_expect_tx(bar(C::B_VFULL + sv), C::VHALF);
+                tma_load_4d(sV + sv * C::VHALF, &tv, bar(C::B_VFULL + sv), 64 * (int)rank, hk, vis.kt(v) * kBN, b);
+                issued = v + 1;
+                if (!(ok = wait_bar(bar(C::B_VFULL + sv), (v / NV) & 1, wc))) break;
+                mbar_arrive_cluster(lead(C::B_GO + v % NK));
+            }
+            if (!ok) {
+                for (int v = issued - NV < 0 ? 0 : issued - NV; v < issued; v++)
+                    drain_bar(bar(C::B_VFULL + v % NV), (v / NV) & 1);
+            }
+        }
+    } else if (warp == 13) {
+        // ------------------------------------------------------------ MMA issuer (even CTA)
+        if (lane == 0 && rank == 0) {
+            constexpr uint32_t idS = idesc_bf16_f32(2 * kBM, kBN, false, false);
+            constexpr uint32_t idSG = idesc_f16_f32(2 * kBM, kBN, false, false);
+            constexpr uint32_t idPV = idesc_bf16_f32(2 * kBM, D, false, true);
+            bool ok = wait_bar_cl(bar(C::B_K0READY), 0, wc);
+            tc_fence_after();
+            auto qk_head = [&](int v, int n) {
+                const uint64_t dk = sdesc_sw128(sK + (v % NK) * C::KHALF, 16, 1024);
+                const uint64_t dq = sdesc_sw128(sQ + n * C::QTILE, 16, 1024);
+                const uint32_t id = vis.remote(v) ? idSG : idS;
+#pragma unroll
+                for (int k = 0; k < D / 16; k++) {
+                    const uint64_t oq = (uint64_t)(((k >> 2) * C::QREG + (k & 3) * 32) >> 4);
+                    const uint64_t ok_ = (uint64_t)(((k >> 2) * C::KREG + (k & 3) * 32) >> 4);
+                    mma2_f16_ss(tmem + 128u * n, dq + oq, dk + ok_, id, k > 0 ? 1u : 0u);
+                }
+                mma2_commit_mc(bar(C::B_SFULL + n), C::BOTH);
+                if (n == 1) {
+                    mma2_commit_mc(bar(C::B_KEMPTY + v % NK), C::BOTH);
+                    if (v == NR - 1) mma2_commit_mc(bar(C::B_QFREE), C::BOTH);
+                }
+            };
+            if (ok)
+                for (int n = 0; n < 2; n++) qk_head(0, n);
+            for (int v = 0; ok && v < T; v++) {
+                const int sv = v % NV;
+                const uint64_t dv = sdesc_sw128(sV + sv * C::VHALF, C::VHALF, 1024);
+                for (int n = 0; n < 2; n++) {
+                    if (n == 0) ok = wait_bar_cl(bar(C::B_GO + v % NK), (v / NK) & 1, wc);
+                    else ok = wait_bar_cl(bar(C::B_PFULL + 1), v & 1, wc);
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int k = 0; k < kBN / 16; k++)
+                        mma2_f16_ts(tmem + 256u + 128u * n, tmem + 128u * n + 8u * k,
+                                    dv + (uint64_t)((k * 2048) >> 4), idPV, (v > 0 || k > 0) ? 1u : 0u);
+                    mma2_commit_mc(bar(C::B_ODONE + n), C::BOTH);
+                    if (n == 1) mma2_commit_mc(bar(C::B_VEMPTY + sv), C::BOTH);
+                    if (v + 1 < T) qk_head(v + 1, n);
+                }
+            }
+            if (!ok) {
+                // no MMA may still run when the CTAs release TMEM and shared memory
+                mma2_commit_mc(bar(C::B_DRAIN), 0x1);
+                drain_bar(bar(C::B_DRAIN), 0);
+            }
+        }
+        __syncwarp();
+    } else if (warp < 8) {
+        // ------------------------------------------------------------ softmax
+        const int n = warp >> 2;  // head slot
+        const int q4 = warp & 3;
+        const int row = 32 * q4 + lane;
+        const int i = i0 + row;
+        const int h = h0 + n;
+        const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+        const uint32_t tS = tmem + lane_base + 128u * n;
+        const uint32_t tO = tmem + lane_base + 256u + 128u * n;
+        const float sc = p.scale_log2;
+        float m_used = -INFINITY, l = 0.f;  // m_used in log2 units
+        bool ok = true;
+        const jl::f32x2 sc2 = jl::f2(sc, sc);
+        for (int v = 0; v < T; v++) {
+            const int kt = vis.kt(v);
+            const bool remote = vis.remote(v);
+            const int j0 = kt * kBN;
+            const bool band = jl::tile_class(i0, j0, kBM, kBN, S, w, g_cls) == jl::kTileBand;
+            const bool masked = band || (j0 + kBN - 1 > i0) || (j0 + kBN > S);
+            auto load_half = [&](int hh, uint32_t (&x)[64]) {
+                tmem_ld32(tS + 64u * hh, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+                tmem_ld32(tS + 64u * hh + 32u, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+                tmem_ld_wait();
+                if (masked) {
+#pragma unroll
+                    for (int e = 0; e < 64; e++) {
+                        const int j = j0 + 64 * hh + e;
+                        bool d = (j > i || j >= S);
+                        if (band) d = d || (remote ? (i - j < w) : (i - j >= w));
+                        if (d) x[e] = 0xff800000u;
+                    }
+                }
+            };
+            auto exp_half = [&](int hh, const uint32_t (&x)[64], jl::f32x2 nm, jl::f32x2 &lsum) {
+#pragma unroll
+                for (int q = 0; q < 2; q++) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; e++) {
+                        const int k2 = 32 * q + 2 * e;
+                        const jl::f32x2 t =
+                            jl::fma2(jl::f2(__uint_as_float(x[k2]), __uint_as_float(x[k2 + 1])), sc2, nm);
+                        float t0, t1;
+                        jl::f2_split(t, t0, t1);
+                        const jl::f32x2 pp = jl::f2(fast_exp2(t0), fast_exp2(t1));
+                        lsum = jl::add2(lsum, pp);
+                        pk[e] = jl::f2_to_bf16x2(pp);
+                    }
+                    tmem_st16(tS + 32u * hh + 16u * q, pk);
+                }
+            };
+            if (!(ok = wait_bar_warp_cl(bar(C::B_SFULL + n), v & 1, wc))) break;
+            tc_fence_after();
+            float m_cur = m_used;
+            jl::f32x2 lsum = jl::f2(0.f, 0.f);
+#pragma unroll 1
+            for (int hh = 0; hh < 2; hh++) {
+                uint32_t x[64];
+                load_half(hh, x);
+                float cm = -INFINITY;
+#pragma unroll
+                for (int e = 0; e < 32; e++)
+                    cm = jl::fmax3(cm, __uint_as_float(x[2 * e]), __uint_as_float(x[2 * e + 1]));
+                cm *= sc;
+                const bool raise = cm > m_cur + kRescaleThreshold;
+                float f = 1.f;
+                if (raise) {
+                    if (m_cur == -INFINITY) {
+                        m_cur = cm;
+                    } else {
+                        const float k = ceilf(cm - m_cur);
+                        m_cur += k;
+                        f = k >= 150.f ? 0.f : ldexpf(1.f, -(int)k);
+                    }
+                }
+                if (hh > 0 && __any_sync(0xffffffffu, raise && f != 1.f)) {
+                    lsum = jl::mul2(lsum, jl::f2(f, f));
+                    tmem_st_wait();
+#pragma unroll 1
+                    for (int c2 = 0; c2 < 2; c2++) {
+                        uint32_t pk[16];
+                        tmem_ld16(tS + 16u * c2, pk);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 16; e++)
+                            pk[e] = jl::f2_to_bf16x2(jl::mul2(jl::bf16x2_to_f2(pk[e]), jl::f2(f, f)));
+                        tmem_st16(tS + 16u * c2, pk);
+                    }
+                }
+                const float m_off = (m_cur == -INFINITY) ? 0.f : m_cur;
+                exp_half(hh, x, jl::f2(-m_off, -m_off), lsum);
+            }
+            const bool moved = m_cur != m_used;
+            const bool need_o = moved && m_used != -INFINITY;
+            const float factor = need_o ? exp2f(m_used - m_cur) : (moved ? 0.f : 1.f);
+            l *= factor;
+            if (v >= 1 && __any_sync(0xffffffffu, need_o)) {
+                const float fo = need_o ? factor : 1.f;
+                if (!(ok = wait_bar_warp_cl(bar(C::B_ODONE + n), (v - 1) & 1, wc))) break;
+                tc_fence_after();
+#pragma unroll 1
+                for (int ch = 0; ch < D / 32; ch++) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + 32u * ch, o);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; e++) o[e] = __float_as_uint(__uint_as_float(o[e]) * fo);
+                    tmem_st32(tO + 32u * ch, o);
+                }
+            }
+            m_used = m_cur;
+            float l0, l1;
+            jl::f2_split(lsum, l0, l1);
+            l += l0 + l1;
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(n == 0 ? lead(C::B_GO + v % NK) : lead(C::B_PFULL + 1));
+        }
+        // ------------------------------------------------------------ epilogue
+        if (ok) ok = wait_bar_warp_cl(bar(C::B_ODONE + n), (T - 1) & 1, wc);
+        if (ok) {
+            tc_fence_after();
+            if (!(l < INFINITY)) jl::record_status(p.status, JL_ERR_GUARD);
+            const float inv_l = 1.f / l;
+            const int il = i - p.pos0;
+            __nv_bfloat16 *orow = p.out + (((size_t)b * p.q_rows + il) * p.Hq + h) * D;
+#pragma unroll 1
+            for (int ch = 0; ch < D / 32; ch++) {
+                uint32_t o[32];
+                tmem_ld32(tO + 32u * ch, o);
+                tmem_ld_wait();
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; e++)
+                    pk[e] = jl::pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
+                if (i < S) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * ch);
+#pragma unroll
+                    for (int q = 0; q < 4; q++)
+                        dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                }
+            }
+            if (i < S) p.lse[((size_t)b * p.Hq + h) * p.lse_stride + il] = (m_used + log2f(l)) * kLn2;
+        }
+    } else {
+        // ------------------------------------------------------------ correction
+        // As in prefill_kernel, for this CTA's half of every K tile: K(u) ready
+        // (landed, and corrected if remote) -> one arrival per warp on the even
+        // CTA's K0READY (u = 0) or GO[(u-1) % NK].  The final arrival (u = T) has
+        // no K tile to order it after GO's phase for tile T-1-NK; the commit that
+        // frees the stage of QK(T-NK) -- issued right after the issuer's wait on
+        // that phase -- does, and it reaches this CTA's KEMPTY.
+        const int t = threadIdx.x - 256;
+        Corrector<D, 128> corq;
+        Corrector<D, 64> cork;
+        if (NR > 0) {
+            corq.init(t, g, pt, rc);
+            cork.init(t, g, pt, rc);
+        }
+        bool ok = wait_bar_warp(bar(C::B_QFULL), 0, wc);
+        if (ok && NR > 0) {
+#pragma unroll 1
+            for (int n = 0; n < 2; n++) corq.run_q(sQ + n * C::QTILE, i0, p.qshift);
+        }
+        for (int u = 0; ok && u <= T; u++) {
+            if (u < T) {
+                const int sk = u % NK;
+                if (!(ok = wait_bar_warp(bar(C::B_KFULL + sk), (u / NK) & 1, wc))) break;
+                if (u < NR) cork.run_k(sK + sk * C::KHALF, u, 64 * (int)rank);
+                if (u == NR && NR > 0 && !(ok = wait_bar_warp(bar(C::B_QFULL), 1, wc))) break;
+                if (u <= NR) fence_proxy_async_smem();
+            }
+            if (u == T && T - 1 >= NK &&
+                !(ok = wait_bar_warp_cl(bar(C::B_KEMPTY + (T - NK) % NK), ((T - NK) / NK) & 1, wc)))
+                break;
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(u == 0 ? lead(C::B_K0READY) : lead(C::B_GO + (u - 1) % NK));
+        }
+    }
+
+    // every MMA has completed (the epilogues waited for the last ones, an
+    // aborting issuer drained them) before either CTA releases TMEM or exits
+    __syncwarp();
+    tc_fence_before();
+    cluster_sync();
+    tc_fence_after();
+    if (warp == 13) tmem_dealloc2(tmem, 512);
+}
+
+int launch_pair(const CUtensorMap &tq, const CUtensorMap &tk64, const CUtensorMap &tv, const Params &p,
+                const jl::PhaseTable &pt, const RotConsts &rc, cudaStream_t st)
+{
+    cudaError_t e = cudaFuncSetAttribute(prefill_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         PairCfg::SMEM);
+    if (e != cudaSuccess) return jl::cuda_status(e);
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3((unsigned)(p.pairs * p.n_qtiles), (unsigned)(p.B * p.Hkv), 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = PairCfg::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return jl::cuda_status(cudaLaunchKernelEx(&cfg, prefill_pair_kernel, tq, tk64, tv, p, pt, rc));
+}
+
+// ---------------------------------------------------------------- few-key rows
+// Rows at positions below kFewKeyRows see fewer than kFewKeyRows keys.  The
+// tile kernel rounds to 16 bits what it feeds the tensor cores: P to bf16
+// (relative error up to 2^-9) while out and lse are normalised by the fp32
+// sum of P, and, in the remote view, the corrected q and k to fp16 (2^-11
+// each, about 4e-4 on one score).  Over many keys these errors average down in
+// out and in the log-sum-exp; over a handful they do not (a row of two keys
+// whose V rows differ by 8 can miss out by 2^-9 * 4 plus its own rounding).
+// This kernel recomputes those rows in fp32 on CUDA cores -- the same
+// definition, key by key -- and overwrites what the tile kernel wrote for
+// them.  Its cost is at most kFewKeyRows rows of at most kFewKeyRows keys per
+// call.
+constexpr int kFewKeyRows = 256;
+constexpr int kFewThreads = 128;
+
+struct FewRowParams {
+    const __nv_bfloat16 *q;  // row 0 at position pos0; batch stride q_rows rows
+    const __nv_bfloat16 *k;  // [B, n_cap, Hkv, D]
+    const __nv_bfloat16 *v;
+    __nv_bfloat16 *out;      // as q
+    float *lse;              // column 0 at position pos0; row stride lse_stride
+    int Hq, Hkv, q_rows, lse_stride, n_cap;
+    int pos0;    // position of q / out / lse row 0
+    int first;   // position of the first row recomputed (block x = 0)
+    int w, g;
+    int qshift;   // added to the query's correction offset
+    int sliding;  // keys with i - j >= w are not attended
+    float scale_log2;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kFewThreads)
+    few_key_rows_kernel(const FewRowParams a, const __grid_constant__ jl::PhaseTable pt)
+{
+    constexpr int HALF = D / 2;
+    __shared__ float sq[D], sqg[D], sc[kFewKeyRows], red[kFewThreads / 32];
+    const int i = a.first + (int)blockIdx.x;  // absolute position of the query row
+    const int h = (int)blockIdx.y, b = (int)blockIdx.z;
+    const int hk = h / (a.Hq / a.Hkv);
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const size_t qrow = ((size_t)b * a.q_rows + (i - a.pos0)) * a.Hq + h;
+    for (int d = t; d < D; d += kFewThreads) sq[d] = __bfloat162float(a.q[qrow * D + d]);
+    __syncthreads();
+    const int di = jl::delta_pos(i, a.g) + a.qshift;
+    for (int d = t; d < HALF; d += kFewThreads) {
+        float sn, cs;
+        jl::phase_sincos(di, pt.f[d], &sn, &cs);
+        sqg[d] = sq[d] * cs - sq[d + HALF] * sn;
+        sqg[d + HALF] = sq[d + HALF] * cs + sq[d] * sn;
+    }
+    __syncthreads();
+    // scores (log2 units) of keys 0..i: exact inside the window, corrected outside
+    for (int j = t; j <= i; j += kFewThreads) {
+        const __nv_bfloat16 *kj = a.k + (((size_t)b * a.n_cap + j) * a.Hkv + hk) * D;
+        float acc = 0.f;
+        if (i - j < a.w || (a.g == 1 && !a.sliding)) {
+            for (int d = 0; d < D; d++) acc = fmaf(sq[d], __bfloat162float(kj[d]), acc);
+        } else if (a.sliding) {
+            acc = -INFINITY;  // outside a sliding window: not attended
+        } else {
+            const int dj = jl::delta_pos(j, a.g);
+            for (int d = 0; d < HALF; d++) {
+                float sn, cs;
+                jl::phase_sincos(dj, pt.f[d], &sn, &cs);
+                const float x = __bfloat162float(kj[d]), y = __bfloat162float(kj[d + HALF]);
+                acc = fmaf(sqg[d], x * cs - y * sn, acc);
+                acc = fmaf(sqg[d + HALF], y * cs + x * sn, acc);
+            }
+        }
+        sc[j] = acc * a.scale_log2;
+    }
+    __syncthreads();
+    // row maximum and sum of 2^(s - m)
+    float m = -INFINITY;
+    for (int j = t; j <= i; j += kFewThreads) m = fmaxf(m, sc[j]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    m = red[0];
+#pragma unroll
+    for (int q = 1; q < kFewThreads / 32; q++) m = fmaxf(m, red[q]);
+    __syncthreads();
+    float l = 0.f;
+    for (int j = t; j <= i; j += kFewThreads) {
+        const float pj = exp2f(sc[j] - m);
+        sc[j] = pj;
+        l += pj;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    if (lane == 0) red[warp] = l;
+    __syncthreads();
+    l = 0.f;
+#pragma unroll
+    for (int q = 0; q < kFewThreads / 32; q++) l += red[q];
+    const float inv_l = 1.f / l;
+    for (int d = t; d < D; d += kFewThreads) {
+        float o = 0.f;
+        for (int j = 0; j <= i; j++)
+            o = fmaf(sc[j], __bfloat162float(a.v[(((size_t)b * a.n_cap + j) * a.Hkv + hk) * D + d]), o);
+        a.out[qrow * D + d] = __float2bfloat16_rn(o * inv_l);
+    }
+    if (t == 0) a.lse[((size_t)b * a.Hq + h) * a.lse_stride + (i - a.pos0)] = (m + log2f(l)) * kLn2;
+}
+
 // ---------------------------------------------------------------- host side
 template <int D, int NH>
 int launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const Params &p,
@@ -769,17 +1347,128 @@ int launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, 
 
 }  // namespace
 
+// Arguments shared by every launch of one prefill call (already validated).
+struct PrefillCall {
+    const void *k, *v;
+    int B, Hq, Hkv, n_cap, D, w;
+    int q_rows, lse_stride;  // batch stride of q / out (rows), row stride of lse
+    int sliding;
+    int pair;  // the two-SM kernel where it applies (JL_PREFILL_CTA_PAIR)
+    jl::PhaseTable pt;
+    float scale_log2;
+    cudaStream_t st;
+};
+
+// One launch: the Sq query rows at positions pos0..pos0+Sq-1 (q, out and lse
+// point at the first of them) over the keys at positions 0..pos0+Sq-1, with
+// group factor g and the query's correction offset shifted by qshift.
+static int prefill_rows(const PrefillCall &c, const void *q, void *out, float *lse, int Sq, int pos0,
+                        int g, int qshift)
+{
+    const int S = pos0 + Sq;
+    const int D = c.D;
+    const long long n_qtiles = ((long long)Sq + kBM - 1) / kBM;
+    if ((long long)c.Hq * n_qtiles > 0x7fffffffLL) return JL_ERR_OVERFLOW;
+    CUtensorMap tq, tk, tv;
+    if (!jl::make_bshd_map(&tq, q, c.B, Sq, c.q_rows, c.Hq, D, 64, 128, true) ||
+        !jl::make_bshd_map(&tk, c.k, c.B, S, c.n_cap, c.Hkv, D, 64, 128, true) ||
+        !jl::make_bshd_map(&tv, c.v, c.B, S, c.n_cap, c.Hkv, D, 64, 128, true))
+        return JL_ERR_CUDA;
+    Params p;
+    p.out = (__nv_bfloat16 *)out;
+    p.lse = lse;
+    p.status = jl::status_word_ptr();
+    p.B = c.B;
+    p.Hq = c.Hq;
+    p.Hkv = c.Hkv;
+    p.S = S;
+    p.Sq = Sq;
+    p.pos0 = pos0;
+    p.w = c.w;
+    p.g = g;
+    p.grp = c.Hq / c.Hkv;
+    p.n_qtiles = (int)n_qtiles;
+    p.q_rows = c.q_rows;
+    p.lse_stride = c.lse_stride;
+    p.qshift = qshift;
+    p.sliding = c.sliding;
+    // two heads of a GQA group per CTA when the group size is even
+    const int nh = (p.grp % 2 == 0) ? 2 : 1;
+    p.pairs = p.grp / nh;
+    p.scale_log2 = c.scale_log2;
+    // step rotations of the correction (rows per step: 16 at D = 128, 32 at D = 64)
+    RotConsts rc;
+    memset(&rc, 0, sizeof(rc));
+    const int rps = 128 / (D / 16);
+    const long long qs = rps / g;
+    rc.uni = (rps % g == 0) ? 1 : 0;
+    for (int d = 0; d < D / 2; d++) {
+        jl::rotation_host(c.pt, d, qs - rps, &rc.ac[d], &rc.as[d]);
+        jl::rotation_host(c.pt, d, qs + 1 - rps, &rc.bc[d], &rc.bs[d]);
+        jl::rotation_host(c.pt, d, 2 * (qs - rps), &rc.a2c[d], &rc.a2s[d]);
+        rc.ans[d] = -rc.as[d];
+        rc.bns[d] = -rc.bs[d];
+        rc.a2ns[d] = -rc.a2s[d];
+    }
+    int rc_launch;
+    if (c.pair && D == 128 && p.grp % 4 == 0) {
+        // four heads per kv head or a multiple: a CTA pair per query tile of four heads
+        CUtensorMap tk64;
+        if (!jl::make_bshd_map(&tk64, c.k, c.B, S, c.n_cap, c.Hkv, D, 64, 64, true)) return JL_ERR_CUDA;
+        rc_launch = launch_pair(tq, tk64, tv, p, c.pt, rc, c.st);
+    } else if (D == 128)
+        rc_launch = nh == 2 ? launch<128, 2>(tq, tk, tv, p, c.pt, rc, c.st) : launch<128, 1>(tq, tk, tv, p, c.pt, rc, c.st);
+    else
+        rc_launch = nh == 2 ? launch<64, 2>(tq, tk, tv, p, c.pt, rc, c.st) : launch<64, 1>(tq, tk, tv, p, c.pt, rc, c.st);
+    if (rc_launch != JL_OK) return rc_launch;
+    // rows below kFewKeyRows are redone in fp32
+    const int few_lo = pos0;
+    const int few_hi = S < kFewKeyRows ? S : kFewKeyRows;
+    if (few_lo < few_hi) {
+        FewRowParams f;
+        f.q = (const __nv_bfloat16 *)q;
+        f.k = (const __nv_bfloat16 *)c.k;
+        f.v = (const __nv_bfloat16 *)c.v;
+        f.out = (__nv_bfloat16 *)out;
+        f.lse = lse;
+        f.Hq = c.Hq;
+        f.Hkv = c.Hkv;
+        f.q_rows = c.q_rows;
+        f.lse_stride = c.lse_stride;
+        f.n_cap = c.n_cap;
+        f.pos0 = pos0;
+        f.first = few_lo;
+        f.w = c.w;
+        f.g = g;
+        f.qshift = qshift;
+        f.sliding = c.sliding;
+        f.scale_log2 = c.scale_log2;
+        dim3 grid((unsigned)(few_hi - few_lo), (unsigned)c.Hq, (unsigned)c.B);
+        if (D == 128) few_key_rows_kernel<128><<<grid, kFewThreads, 0, c.st>>>(f, c.pt);
+        else few_key_rows_kernel<64><<<grid, kFewThreads, 0, c.st>>>(f, c.pt);
+        return jl::cuda_status(cudaGetLastError());
+    }
+    return JL_OK;
+}
+
 // Prefill of Sq queries at positions n_past..n_past+Sq-1 over the keys at
 // positions 0..n_past+Sq-1 (k / v: [B, n_cap, Hkv, D], rows past the keys
-// are never read), s = n_past + Sq.
+// are never read), s = n_past + Sq, with the variant flags of the header.
 static int prefill_impl(const void *q, const void *k, const void *v, void *out, float *lse, int B, int Hq,
-                 int Hkv, int Sq, int n_past, int n_cap, int D, int L_pre, int w, double theta,
-                 void *stream)
+                        int Hkv, int Sq, int n_past, int n_cap, int D, int L_pre, int w, double theta,
+                        unsigned flags, void *stream)
 {
     if (!q || !k || !v || !out || !lse) return JL_ERR_ARG;
     if (B < 1 || Hq < 1 || Hkv < 1 || Sq < 1 || n_past < 0 || L_pre < 1 || w < 1 ||
         !(theta > 0.0) || Hq % Hkv != 0)
         return JL_ERR_ARG;
+    if (flags & ~(unsigned)(JL_VARIANT_PER_QUERY_G | JL_VARIANT_SLIDING | JL_VARIANT_QUERY_SHIFT |
+                            JL_PREFILL_CTA_PAIR))
+        return JL_ERR_ARG;
+    const bool pair = (flags & JL_PREFILL_CTA_PAIR) != 0;
+    flags &= ~(unsigned)JL_PREFILL_CTA_PAIR;
+    if ((flags & JL_VARIANT_SLIDING) && flags != JL_VARIANT_SLIDING) return JL_ERR_ARG;
+    if ((flags & JL_VARIANT_PER_QUERY_G) && (flags & JL_VARIANT_QUERY_SHIFT)) return JL_ERR_UNSUPPORTED;
     if ((long long)n_past + Sq > 0x7fffffffLL) return JL_ERR_OVERFLOW;
     const int S = n_past + Sq;
     if (n_cap < S) return JL_ERR_ARG;
@@ -790,58 +1479,55 @@ static int prefill_impl(const void *q, const void *k, const void *v, void *out, 
     if ((long long)B * Sq * Hq * D > ((long long)1 << 46) ||
         (long long)B * n_cap * Hkv * D > ((long long)1 << 46))
         return JL_ERR_OVERFLOW;
-    const long long n_qtiles = ((long long)Sq + kBM - 1) / kBM;
-    if ((long long)B * Hkv > 65535 || (long long)Hq * n_qtiles > 0x7fffffffLL) return JL_ERR_OVERFLOW;
-    jl::PhaseTable pt;
-    if (!jl::make_phase_table(&pt, D, theta)) return JL_ERR_ARG;
-    CUtensorMap tq, tk, tv;
-    if (!jl::make_bshd_map(&tq, q, B, Sq, Sq, Hq, D, 64, 128, true) ||
-        !jl::make_bshd_map(&tk, k, B, S, n_cap, Hkv, D, 64, 128, true) ||
-        !jl::make_bshd_map(&tv, v, B, S, n_cap, Hkv, D, 64, 128, true))
-        return JL_ERR_CUDA;
-    Params p;
-    p.out = (__nv_bfloat16 *)out;
-    p.lse = lse;
-    p.status = jl::status_word_ptr();
-    p.B = B;
-    p.Hq = Hq;
-    p.Hkv = Hkv;
-    p.S = S;
-    p.Sq = Sq;
-    p.pos0 = n_past;
-    p.w = w;
-    p.g = (int)jl::group_factor_host(S, L_pre);
-    p.grp = Hq / Hkv;
-    p.n_qtiles = (int)n_qtiles;
-    // two heads of a GQA group per CTA when the group size is even
-    const int nh = (p.grp % 2 == 0) ? 2 : 1;
-    p.pairs = p.grp / nh;
-    p.scale_log2 = (float)(1.0 / sqrt((double)D) * 1.4426950408889634);
-    // step rotations of the correction (rows per step: 16 at D = 128, 32 at D = 64)
-    RotConsts rc;
-    memset(&rc, 0, sizeof(rc));
-    const int rps = 128 / (D / 16);
-    const long long qs = rps / p.g;
-    rc.uni = (rps % p.g == 0) ? 1 : 0;
-    for (int d = 0; d < D / 2; d++) {
-        jl::rotation_host(pt, d, qs - rps, &rc.ac[d], &rc.as[d]);
-        jl::rotation_host(pt, d, qs + 1 - rps, &rc.bc[d], &rc.bs[d]);
-        jl::rotation_host(pt, d, 2 * (qs - rps), &rc.a2c[d], &rc.a2s[d]);
-        rc.ans[d] = -rc.as[d];
-        rc.bns[d] = -rc.bs[d];
-        rc.a2ns[d] = -rc.a2s[d];
+    if ((long long)B * Hkv > 65535 || Hq > 65535) return JL_ERR_OVERFLOW;
+    long long g_call = jl::group_factor_host(S, L_pre);
+    int qshift = 0;
+    if (flags & JL_VARIANT_QUERY_SHIFT) {
+        g_call = jl::group_factor_shift_host(S, L_pre, w);
+        if (g_call < 1) return JL_ERR_ARG;  // no g keeps the shifted distances inside L_pre
+        qshift = (int)(w - w / g_call);
     }
-    cudaStream_t st = (cudaStream_t)stream;
-    if (D == 128)
-        return nh == 2 ? launch<128, 2>(tq, tk, tv, p, pt, rc, st) : launch<128, 1>(tq, tk, tv, p, pt, rc, st);
-    return nh == 2 ? launch<64, 2>(tq, tk, tv, p, pt, rc, st) : launch<64, 1>(tq, tk, tv, p, pt, rc, st);
+    if (g_call > 0x7fffffffLL) return JL_ERR_OVERFLOW;
+    PrefillCall c;
+    c.k = k;
+    c.v = v;
+    c.B = B;
+    c.Hq = Hq;
+    c.Hkv = Hkv;
+    c.n_cap = n_cap;
+    c.D = D;
+    c.w = w;
+    c.q_rows = Sq;
+    c.lse_stride = Sq;
+    c.sliding = (flags & JL_VARIANT_SLIDING) ? 1 : 0;
+    c.pair = pair ? 1 : 0;
+    if (!jl::make_phase_table(&c.pt, D, theta)) return JL_ERR_ARG;
+    c.scale_log2 = (float)(1.0 / sqrt((double)D) * 1.4426950408889634);
+    c.st = (cudaStream_t)stream;
+    if (c.sliding) return prefill_rows(c, q, out, lse, Sq, n_past, 1, 0);
+    if (!(flags & JL_VARIANT_PER_QUERY_G)) return prefill_rows(c, q, out, lse, Sq, n_past, (int)g_call, qshift);
+    // per-query group factor: row i has s = i + 1, so g = ceil((i + 1) / L_pre) is
+    // constant on the rows [(g-1) L_pre, g L_pre); each such range is one launch whose
+    // rows see the keys before them -- the chunk of a prefill of length g L_pre
+    const size_t row_bytes = (size_t)Hq * D * sizeof(__nv_bfloat16);
+    for (int a = n_past; a < S;) {
+        const long long g = jl::group_factor_host((long long)a + 1, L_pre);
+        const long long end_ll = g * (long long)L_pre;
+        const int b = end_ll < S ? (int)end_ll : S;
+        const size_t r = (size_t)(a - n_past);
+        const int rc = prefill_rows(c, (const char *)q + r * row_bytes, (char *)out + r * row_bytes, lse + r,
+                                    b - a, a, (int)g, 0);
+        if (rc != JL_OK) return rc;
+        a = b;
+    }
+    return JL_OK;
 }
 
 extern "C" int jl_bifocal_prefill(const void *q, const void *k, const void *v, void *out, float *lse,
                                   int B, int Hq, int Hkv, int S, int D, int L_pre, int w,
                                   double theta, void *stream)
 {
-    return prefill_impl(q, k, v, out, lse, B, Hq, Hkv, S, 0, S, D, L_pre, w, theta, stream);
+    return prefill_impl(q, k, v, out, lse, B, Hq, Hkv, S, 0, S, D, L_pre, w, theta, 0u, stream);
 }
 
 extern "C" int jl_bifocal_prefill_chunk(const void *q, const void *k_cache, const void *v_cache,
@@ -850,5 +1536,13 @@ extern "C" int jl_bifocal_prefill_chunk(const void *q, const void *k_cache, cons
                                         void *stream)
 {
     return prefill_impl(q, k_cache, v_cache, out, lse, B, Hq, Hkv, S_new, n_past, n_cap, D, L_pre, w,
-                        theta, stream);
+                        theta, 0u, stream);
+}
+
+extern "C" int jl_bifocal_prefill_ex(const void *q, const void *k_cache, const void *v_cache, void *out,
+                                     float *lse, int B, int Hq, int Hkv, int S_new, int n_past, int n_cap,
+                                     int D, int L_pre, int w, double theta, unsigned flags, void *stream)
+{
+    return prefill_impl(q, k_cache, v_cache, out, lse, B, Hq, Hkv, S_new, n_past, n_cap, D, L_pre, w,
+                        theta, flags, stream);
 }

@@ -283,5 +283,144 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// ------------------------------------------------------------------ clusters of two CTAs
+// Used by kernels launched as clusters of two CTAs that pair their SMs on
+// one tcgen05 MMA (cta_group::2): A rows split between the CTAs, B split
+// along N, D in each CTA's own TMEM.
+
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address in the cluster shared window of the same shared variable in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+// Arrive on an mbarrier given by its cluster-window address (own CTA or peer),
+// releasing this thread's prior writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// try_wait that acquires at cluster scope (arrivals may come from the peer CTA).
+__device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Single-thread bounded wait, cluster-scope acquire (see wait_bar).
+__device__ __forceinline__ bool wait_bar_cl(uint32_t bar, uint32_t parity, const WaitCtx &w)
+{
+    if (mbar_try_wait_cl(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int k = 0; k < 32; k++)
+            if (mbar_try_wait_cl(bar, parity)) return true;
+        if (*w.abort) return false;
+        if (globaltimer_ns() - t0 > w.limit_ns) {
+            record_status(w.status, JL_ERR_TIMEOUT);
+            *w.abort = 1;
+            return false;
+        }
+    }
+}
+
+// Warp-uniform bounded wait, cluster-scope acquire (see wait_bar_warp).
+__device__ __forceinline__ bool wait_bar_warp_cl(uint32_t bar, uint32_t parity, const WaitCtx &w)
+{
+    bool done = mbar_try_wait_cl(bar, parity);
+    if (__all_sync(0xffffffffu, done)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    while (true) {
+        if (!done) done = mbar_try_wait_cl(bar, parity);
+        if (__all_sync(0xffffffffu, done)) return true;
+        int stop = 0;
+        if ((threadIdx.x & 31) == 0) {
+            if (*w.abort) stop = 1;
+            else if (globaltimer_ns() - t0 > w.limit_ns) {
+                record_status(w.status, JL_ERR_TIMEOUT);
+                *w.abort = 1;
+                stop = 1;
+            }
+        }
+        if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+    }
+}
+
+// Every thread of both CTAs: arrive and wait on the cluster barrier.
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// TMEM allocation shared by the CTA pair: one warp of EACH CTA executes these.
+__device__ __forceinline__ void tmem_alloc2(uint32_t dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish2()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Pair MMA, issued by one thread of the even CTA: D (each CTA's TMEM, 128
+// lanes) (+)= A[smem, both CTAs] * B[smem, N split between the CTAs]^T.
+__device__ __forceinline__ void mma2_f16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Pair MMA with A from each CTA's TMEM.
+__device__ __forceinline__ void mma2_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on the mbarrier at `bar` (a CTA-local offset) in every CTA of
+// ctamask when all pair MMAs this thread issued so far have completed.
+__device__ __forceinline__ void mma2_commit_mc(uint32_t bar, uint16_t ctamask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"(ctamask)
+        : "memory");
+}
+
 }  // namespace ptx
 }  // namespace jl
