@@ -590,8 +590,10 @@ def run_case(args):
         lse = torch.empty((1, cfg["Hq"], args.S), dtype=torch.float32, device=dev)
         L = args.L if args.L > 0 else cfg["L_pre"]
 
+        flags = jl.JL_PREFILL_CTA_PAIR if args.pair else 0
+
         def call():
-            jl.jl_bifocal_prefill(q, k, v, L, cfg["w"], cfg["theta"], out=out, lse=lse, stream=stream)
+            jl.jl_bifocal_prefill_ex(q, k, v, 0, L, cfg["w"], cfg["theta"], flags, out=out, lse=lse, stream=stream)
         flops = prefill_flops(1, cfg["Hq"], cfg["D"], args.S)
     else:
         n = args.n
@@ -629,6 +631,8 @@ def main():
     ap.add_argument("--n", type=int, default=8192)
     ap.add_argument("--L", type=int, default=0)
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--pair", action="store_true",
+                    help="--case prefill: the two-SM tile kernel (JL_PREFILL_CTA_PAIR)")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)

@@ -256,9 +256,13 @@ int jl_bifocal_prefill_ex(const void *q, const void *k_cache, const void *v_cach
 size_t jl_bifocal_decode_workspace_size(int B, int Hq, int Hkv, int n, int D);
 
 /*
- * Bifocal single-token decode over an exact-RoPE bf16 KV cache (split-KV,
- * fp32 arithmetic on CUDA cores; a non-finite score is reported as
- * JL_ERR_GUARD in the device status word).
+ * Bifocal single-token decode over an exact-RoPE bf16 KV cache (split-KV; a
+ * non-finite score is reported as JL_ERR_GUARD in the device status word).
+ * Numerics: at D = 128 and n >= 256 the scores and P.V run on the tensor
+ * cores (bf16 operands for exact keys, fp16 for corrected ones as in the
+ * prefill, fp32 accumulation, P rounded to bf16 for P.V with out normalised
+ * by the sum of the rounded P and lse by the fp32 sum); shorter caches and
+ * D = 64 use fp32 arithmetic on CUDA cores throughout.
  * Kernels exist for GQA group sizes Hq / Hkv in {1, 2, 4, 8}; any other group
  * size returns JL_ERR_UNSUPPORTED (this also holds for the paged and the
  * no-allocation variants).
@@ -316,7 +320,7 @@ int jl_bifocal_decode_ex(const void *q, const void *k_cache, const void *v_cache
  *            status word (the call never reads past the table or the plan)
  *   out      device bf16 [B, Hq, D];  lse device fp32 [B, Hq]
  *   page_size  a multiple of 64 (the kernel's key block); max_pages * page_size
- *            >= max_n (host: the longest sequence, sizes the split plan)
+ *            >= max_n (host: a bound on every length; longer ones are clamped)
  *   workspace  as for jl_bifocal_decode, at least
  *            jl_bifocal_decode_paged_workspace_size(B, Hq, Hkv, max_n, D) bytes
  * Rows of a sequence's last page past n_b are never used, whatever they hold.
@@ -324,9 +328,12 @@ int jl_bifocal_decode_ex(const void *q, const void *k_cache, const void *v_cache
  * JL_ERR_WORKSPACE or JL_ERR_CUDA.
  */
 /*
- * Workspace bytes jl_bifocal_decode_paged needs: its split plan is sized for
- * the longest sequence (max_n) alone, since a batch may hold one long and many
- * short sequences.  0 on bad sizes.
+ * Workspace bytes jl_bifocal_decode_paged needs.  The kernel shares a fixed
+ * number of CTAs per kv head (about two per SM) among the sequences in
+ * proportion to their lengths, which it reads on the device, so a batch of one
+ * long and many short sequences keeps every CTA equally busy; the workspace
+ * holds that many partial results per (sequence, head) and does not depend on
+ * the lengths.  0 on bad sizes.
  */
 size_t jl_bifocal_decode_paged_workspace_size(int B, int Hq, int Hkv, int max_n, int D);
 

@@ -1,5 +1,7 @@
 """Batched decode over a paged cache with one length per sequence
-(jl_bifocal_decode_paged), against the fp64 oracle.
+(jl_bifocal_decode_paged), against the fp64 oracle.  The kernel splits the
+batch's keys over its CTAs in proportion to the sequences' lengths, reading
+the lengths on the device.
 
 Every sequence b has its own length n_b and so its own g = g(n_b, L) (the
 group factor follows the current length: ResearchPod summary, "every
@@ -61,6 +63,8 @@ def _paged_case(jl, orc, dev, lens, Hq, Hkv, D, page_size, L, w, seed, spare_pag
     ((3000, 64, 4097, 130), 16, 8, 128, 128, 1000, 64),  # page 128, g = 3, 1, 5, 1
     ((777, 2048), 8, 4, 64, 64, 300, 100),            # D = 64, grp = 2, g = 3, 7
     ((9000,), 32, 8, 128, 64, 9000, 4096),            # n <= L: plain RoPE
+    # twelve sequences: the device shares the CTAs out in proportion to length
+    ((5, 77, 300, 4097, 12000, 64, 1, 2000, 700, 9000, 128, 33), 32, 8, 128, 64, 1000, 256),
 ])
 def test_paged_decode_parity(jl, orc, dev, lens, Hq, Hkv, D, page_size, L, w):
     _paged_case(jl, orc, dev, list(lens), Hq, Hkv, D, page_size, L, w, seed=21)

@@ -136,6 +136,24 @@ def test_decode_parity_small(jl, orc, dev, B, Hq, Hkv, n, n_cap, D, L, w):
     _decode_case(jl, orc, dev, B, Hq, Hkv, n, n_cap, D, L, w, 1e6, seed=3)
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,n,n_cap,L,w", [
+    (1, 8, 8, 256, 256, 64, 100),          # the shortest cache on the tensor cores; grp 1, g = 4
+    (1, 16, 2, 257, 300, 64, 128),         # grp 8, one key past a tile, edge inside tile 1
+    (1, 16, 2, 257, 300, 64, 129),         # edge on a tile boundary: no crossed tile
+    (1, 4, 1, 700, 700, 100, 1),           # w = 1: only the last key exact, g = 7
+    (2, 32, 8, 1500, 1600, 400, 300),      # B = 2, g = 4, edge inside a middle tile
+    (1, 8, 2, 5000, 5000, 1000, 37),       # grp 4, g = 5 (not a divisor of 16), many splits
+    (1, 4, 2, 20000, 20000, 3000, 2500),   # grp 2, g = 7, splits of several tiles
+    (1, 32, 8, 40000, 40000, 32768, 4096),  # g = 2
+    (4, 32, 8, 9000, 9000, 4096, 1024),    # B = 4: four splits per (batch, kv head)
+    (20, 16, 8, 600, 600, 128, 200),       # 160 (batch, kv head) pairs: one split each
+])
+def test_decode_tensor_core_path(jl, orc, dev, B, Hq, Hkv, n, n_cap, L, w):
+    """Head dimension 128 and n >= 256 take the tcgen05 kernel: tile classes
+    (remote, crossed by the window edge, exact), group sizes, split counts."""
+    _decode_case(jl, orc, dev, B, Hq, Hkv, n, n_cap, 128, L, w, 1e6, seed=11)
+
+
 @pytest.mark.parametrize("n", [8192, 32768, 131072])
 def test_decode_parity_benchmark_sizes(jl, orc, dev, n):
     """Single-batch decode, Hq=32, Hkv=8, D=128, L=32768, w=4096, theta=1e6 (g = 1, 1, 4)."""
@@ -223,8 +241,12 @@ def test_decode_matches_last_prefill_row(jl, dev):
     ("qwen3-8b 128K", 1, 32, 8, 131072, 32768, 4096, 2),
 ])
 def test_prefill_benchmark_configs_sampled(jl, orc, dev, name, B, Hq, Hkv, S, L, w, seed):
+    """Run in full; checked on the rule-edge rows and on one seeded row of
+    every 128-row query tile (512 / 1024 tiles), every head."""
     g = orc.group_factor(S, L)
-    rows = helpers.sample_rows(S, L, w, g, n_random=24, seed=seed)
+    rng = np.random.default_rng(seed)
+    per_tile = np.arange(0, S, 128) + rng.integers(0, 128, size=S // 128)
+    rows = np.unique(np.concatenate([helpers.sample_rows(S, L, w, g, n_random=0), per_tile]))
     _prefill_case(jl, orc, dev, B, Hq, Hkv, S, 128, L, w, 1e6, seed=seed, rows=rows)
 
 

@@ -31,6 +31,7 @@
 
 #include "jl_common.cuh"
 #include "sm100_ptx.cuh"
+#include "corrector.cuh"
 
 namespace {
 
@@ -67,13 +68,29 @@ struct DecodeArgs {
     // pages' row count, table width and the pretrained window (g per sequence)
     const int *seq_lens;     // [B]
     const int *block_table;  // [B, max_pages]
-    int page_size, max_pages, num_pages, L;
+    int page_size, max_pages, num_pages, L, B;
 };
 
 // Named barrier over the compute warps only (the producer warp never joins).
 __device__ __forceinline__ void compute_sync()
 {
     asm volatile("bar.sync 1, %0;" ::"n"(kCompute) : "memory");
+}
+
+// The same barrier, returning whether `v` holds in every compute thread: a
+// wait that gave up in one warp makes all of them leave together.
+__device__ __forceinline__ bool compute_sync_and(bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "n"(kCompute)
+        : "memory");
+    return r != 0;
 }
 
 template <int D, int GRP>
@@ -87,7 +104,7 @@ struct DecCfg {
     static constexpr int OFF_ST = OFF_SC + GRP * kKB * 4;     // fp32 m[GRP], l[GRP], fac[GRP]
     static constexpr int OFF_MW = OFF_ST + 3 * GRP * 4 + 16;  // merge weights [GRP][256]
     static constexpr int OFF_BAR = (OFF_MW + GRP * 256 * 4 + 15) / 16 * 16;
-    static constexpr int SMEM = OFF_BAR + 2 * kNS * 8 + 16;
+    static constexpr int SMEM = OFF_BAR + 2 * kNS * 8 + 32;  // + abort, last, the paged plan
     // end-of-chunk reduction buffer [KPS3][GRP][D] fp32 aliases the K/V ring
     static constexpr int VC = D / 8, KPS3 = kCompute / VC;
     static_assert(KPS3 * GRP * D * 4 <= 2 * kNS * BLOCK_BYTES, "reduction buffer");
@@ -96,8 +113,96 @@ struct DecCfg {
 // PAGED: the keys of sequence b live in pages of a shared pool, page p of it
 // at block_table[b][p]; its length n_b comes from seq_lens[b] and sets its own
 // g.  Otherwise the cache is [B, n_cap, Hkv, D] and every sequence has length n.
+// Resident CTAs per SM the kernel is built for: two, or one for eight heads
+// per kv head, whose per-thread accumulators need more than the 168
+// registers two CTAs of 160 threads leave.
+template <int GRP>
+struct DecOcc {
+    static constexpr int CTAS = GRP <= 4 ? 2 : 1;
+};
+
+// The end of a split: once its partial statistics are written, the last CTA
+// of the (batch, kv head) to finish merges all ns of them into out and lse
+// and resets the arrival counter.  Run by the 128 threads of the compute
+// group (thread indices 0..127); mw, st_m and st_l are shared scratch of
+// GRP * 256, GRP and GRP floats.
+template <int D, int GRP>
+__device__ void ticket_and_merge(const DecodeArgs &a, int b, int hk, int ns, int stride, float *mw,
+                                 float *st_m, float *st_l, volatile int &s_last)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const size_t hq0 = (size_t)b * a.Hq + (size_t)hk * GRP;
+    __threadfence();
+    compute_sync();
+    if (tid == 0) {
+        const int ticket = atomicAdd(&a.counters[b * a.Hkv + hk], 1);
+        s_last = (ticket == ns - 1);
+    }
+    compute_sync();
+    if (!s_last) return;
+    __threadfence();
+
+    // ---- last CTA of this (b, kv head): merge the partial statistics
+    // weights w_s = 2^(m_s - M) with M = max m_s; L = sum l_s w_s
+    for (int h = warp; h < GRP; h += kCompute / 32) {
+        const float *ml = a.part_ml + (hq0 + h) * stride * 2;
+        float m = -INFINITY;
+        for (int q = lane; q < ns; q += 32) m = fmaxf(m, __ldcg(ml + 2 * q));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const float off = (m == -INFINITY) ? 0.f : m;
+        float L = 0.f;
+        for (int q = lane; q < ns; q += 32) {
+            const float wgt = exp2f(__ldcg(ml + 2 * q) - off);
+            mw[h * 256 + q] = wgt;
+            L += wgt * __ldcg(ml + 2 * q + 1);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        if (lane == 0) {
+            st_m[h] = m;
+            st_l[h] = L;
+        }
+    }
+    compute_sync();
+    // each thread: 4 consecutive dims of one head, 8 splits' loads in flight
+    for (int t = tid; t < GRP * D / 4; t += kCompute) {
+        const int h = (4 * t) / D, d = (4 * t) % D;
+        const float *po = a.part_o + (hq0 + h) * stride * D + d;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        int q = 0;
+        for (; q + 8 <= ns; q += 8) {
+            float4 x[8];
+#pragma unroll
+            for (int u = 0; u < 8; u++) x[u] = __ldcg(reinterpret_cast<const float4 *>(po + (size_t)(q + u) * D));
+#pragma unroll
+            for (int u = 0; u < 8; u++) {
+                const float wgt = mw[h * 256 + q + u];
+                o.x = fmaf(wgt, x[u].x, o.x);
+                o.y = fmaf(wgt, x[u].y, o.y);
+                o.z = fmaf(wgt, x[u].z, o.z);
+                o.w = fmaf(wgt, x[u].w, o.w);
+            }
+        }
+        for (; q < ns; q++) {
+            const float4 x = __ldcg(reinterpret_cast<const float4 *>(po + (size_t)q * D));
+            const float wgt = mw[h * 256 + q];
+            o.x = fmaf(wgt, x.x, o.x);
+            o.y = fmaf(wgt, x.y, o.y);
+            o.z = fmaf(wgt, x.z, o.z);
+            o.w = fmaf(wgt, x.w, o.w);
+        }
+        const float inv = 1.f / st_l[h];
+        __nv_bfloat16 *dst = a.out + (hq0 + h) * D + d;
+        *reinterpret_cast<uint2 *>(dst) = make_uint2(jl::pack_bf16x2(o.x * inv, o.y * inv),
+                                                     jl::pack_bf16x2(o.z * inv, o.w * inv));
+    }
+    if (tid < GRP) a.lse[hq0 + tid] = (st_m[tid] + log2f(st_l[tid])) * kLn2;
+    if (tid == 0) a.counters[b * a.Hkv + hk] = 0;  // ready for the next call
+}
+
 template <int D, int GRP, bool PAGED>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, DecOcc<GRP>::CTAS)
     decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                   const DecodeArgs a, const __grid_constant__ jl::PhaseTable pt,
                   const __grid_constant__ DecRot rot)
@@ -127,21 +232,62 @@ __global__ void __launch_bounds__(kThreads, 2)
     const WaitCtx wc{a.status, abort_flag};
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+    const int hk = blockIdx.y;
+    // this CTA's sequence b, its split, the sequence's split count ns, and the
+    // split capacity of the partial-statistics layout
+    int b = blockIdx.z, split = blockIdx.x, ns = a.splits, chunk = a.chunk;
+    const int stride = a.splits;
     int n = a.n, g = a.g;
     if constexpr (PAGED) {
-        // a length the plan or the page table cannot cover is clamped (never
-        // read past either) and reported
-        const int n_lim = min(a.max_pages * a.page_size, a.splits * a.chunk);
-        n = a.seq_lens[b];
-        if (n < 1 || n > n_lim) {
-            if (tid == 0 && split == 0 && hk == 0) jl::record_status(a.status, JL_ERR_GUARD);
-            n = min(max(n, 1), n_lim);
+        // Splits in proportion to the sequences' lengths: one chunk size for
+        // the whole batch from its total key count, so every CTA of the grid
+        // (a.splits per kv head, plus at most one more per sequence) has about
+        // the same number of keys.  Lengths outside [1, min(max_n, what the
+        // page table covers)] are clamped (never read past the table) and
+        // reported.
+        volatile int *s_plan = reinterpret_cast<volatile int *>(smem + C::OFF_BAR + 2 * kNS * 8 + 8);
+        if (tid == 0) {
+            const int n_lim = min(a.max_pages * a.page_size, a.n);
+            long long tot = 0;
+            bool bad = false;
+            for (int s = 0; s < a.B; s++) {
+                const int ls = a.seq_lens[s];
+                bad = bad || ls < 1 || ls > n_lim;
+                tot += min(max(ls, 1), n_lim);
+            }
+            if (bad && blockIdx.x == 0 && hk == 0) jl::record_status(a.status, JL_ERR_GUARD);
+            long long ch = (tot + a.splits - 1) / a.splits;
+            ch = (ch + kKB - 1) / kKB * kKB;
+            int bb = -1, sp = 0, nsb = 0, nb = 0, cum = 0;
+            for (int s = 0; s < a.B; s++) {
+                const int ls = min(max(a.seq_lens[s], 1), n_lim);
+                const int sb = (int)((ls + ch - 1) / ch);
+                if ((int)blockIdx.x < cum + sb) {
+                    bb = s;
+                    sp = (int)blockIdx.x - cum;
+                    nsb = sb;
+                    nb = ls;
+                    break;
+                }
+                cum += sb;
+            }
+            s_plan[0] = bb;
+            s_plan[1] = sp;
+            s_plan[2] = nsb;
+            s_plan[3] = nb;
+            s_plan[4] = (int)ch;
         }
+        __syncthreads();
+        b = s_plan[0];
+        if (b < 0) return;  // past the last sequence's splits: no work
+        split = s_plan[1];
+        ns = s_plan[2];
+        n = s_plan[3];
+        chunk = s_plan[4];
         g = (n <= a.L) ? 1 : (n - 1) / a.L + 1;
     }
-    const int j_begin = split * a.chunk;
-    const int j_end = min(n, j_begin + a.chunk);
+    const int j_begin = split * chunk;
+    const int j_end = min(n, j_begin + chunk);
     const int nblk = (j_end - j_begin + kKB - 1) / kKB;
     const int j_split = (g > 1) ? max(0, n - a.w) : 0;  // keys below are remote
 
@@ -414,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     compute_sync();
     const size_t hq0 = (size_t)b * a.Hq + (size_t)hk * GRP;
-    if (a.splits == 1) {
+    if (ns == 1) {
         for (int t = tid; t < GRP * D; t += kCompute) {
             const int h = t / D, d = t % D;
             float o = 0.f;
@@ -430,83 +576,459 @@ __global__ void __launch_bounds__(kThreads, 2)
         float o = 0.f;
 #pragma unroll
         for (int q = 0; q < KPS3; q++) o += red[(q * GRP + h) * D + d];
-        a.part_o[((hq0 + h) * a.splits + split) * D + d] = o;
+        a.part_o[((hq0 + h) * stride + split) * D + d] = o;
     }
     if (tid < GRP) {
-        a.part_ml[((hq0 + tid) * a.splits + split) * 2 + 0] = st_m[tid];
-        a.part_ml[((hq0 + tid) * a.splits + split) * 2 + 1] = st_l[tid];
+        a.part_ml[((hq0 + tid) * stride + split) * 2 + 0] = st_m[tid];
+        a.part_ml[((hq0 + tid) * stride + split) * 2 + 1] = st_l[tid];
     }
-    __threadfence();
-    compute_sync();
-    if (tid == 0) {
-        const int ticket = atomicAdd(&a.counters[b * a.Hkv + hk], 1);
-        s_last = (ticket == a.splits - 1);
-    }
-    compute_sync();
-    if (!s_last) return;
-    __threadfence();
-
-    // ---- last CTA of this (b, kv head): merge the partial statistics
-    // weights w_s = 2^(m_s - M) with M = max m_s; L = sum l_s w_s
-    for (int h = warp; h < GRP; h += kCompute / 32) {
-        const float *ml = a.part_ml + (hq0 + h) * a.splits * 2;
-        float m = -INFINITY;
-        for (int q = lane; q < a.splits; q += 32) m = fmaxf(m, __ldcg(ml + 2 * q));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        const float off = (m == -INFINITY) ? 0.f : m;
-        float L = 0.f;
-        for (int q = lane; q < a.splits; q += 32) {
-            const float wgt = exp2f(__ldcg(ml + 2 * q) - off);
-            mw[h * 256 + q] = wgt;
-            L += wgt * __ldcg(ml + 2 * q + 1);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-        if (lane == 0) {
-            st_m[h] = m;
-            st_l[h] = L;
-        }
-    }
-    compute_sync();
-    // each thread: 4 consecutive dims of one head, 8 splits' loads in flight
-    for (int t = tid; t < GRP * D / 4; t += kCompute) {
-        const int h = (4 * t) / D, d = (4 * t) % D;
-        const float *po = a.part_o + (hq0 + h) * a.splits * D + d;
-        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-        int q = 0;
-        for (; q + 8 <= a.splits; q += 8) {
-            float4 x[8];
-#pragma unroll
-            for (int u = 0; u < 8; u++) x[u] = __ldcg(reinterpret_cast<const float4 *>(po + (size_t)(q + u) * D));
-#pragma unroll
-            for (int u = 0; u < 8; u++) {
-                const float wgt = mw[h * 256 + q + u];
-                o.x = fmaf(wgt, x[u].x, o.x);
-                o.y = fmaf(wgt, x[u].y, o.y);
-                o.z = fmaf(wgt, x[u].z, o.z);
-                o.w = fmaf(wgt, x[u].w, o.w);
-            }
-        }
-        for (; q < a.splits; q++) {
-            const float4 x = __ldcg(reinterpret_cast<const float4 *>(po + (size_t)q * D));
-            const float wgt = mw[h * 256 + q];
-            o.x = fmaf(wgt, x.x, o.x);
-            o.y = fmaf(wgt, x.y, o.y);
-            o.z = fmaf(wgt, x.z, o.z);
-            o.w = fmaf(wgt, x.w, o.w);
-        }
-        const float inv = 1.f / st_l[h];
-        __nv_bfloat16 *dst = a.out + (hq0 + h) * D + d;
-        *reinterpret_cast<uint2 *>(dst) = make_uint2(jl::pack_bf16x2(o.x * inv, o.y * inv),
-                                                     jl::pack_bf16x2(o.z * inv, o.w * inv));
-    }
-    if (tid < GRP) a.lse[hq0 + tid] = (st_m[tid] + log2f(st_l[tid])) * kLn2;
-    if (tid == 0) a.counters[b * a.Hkv + hk] = 0;  // ready for the next call
+    ticket_and_merge<D, GRP>(a, b, hk, ns, stride, mw, st_m, st_l, s_last);
 }
 
-// Split plan: as many CTAs as the kernel keeps resident (two per SM: shared
-// memory and registers allow two), at most 256 splits per (batch, kv head),
+// ---------------------------------------------------------------- tensor-core decode
+// The same split-KV decode with the dot products and P.V on the tensor core
+// (head dimension 128, contiguous cache).  A CTA streams its chunk of one kv
+// head's keys in 128-key tiles and computes S^T = K Q^T (M = 128 keys, N = 16
+// columns holding the GRP query heads) and O^T += V^T P^T (M = 128 dims, the
+// V tile read as an MN-major A operand), accumulators in TMEM.  Remote tiles
+// are rotated in place by the correction warps (fp16 operands, the corrected
+// query on the other side); the tile the window edge crosses is scored twice,
+// exactly before the correction rotates it and aliased after.  What is left
+// on the CUDA cores per key is the correction and a handful of softmax
+// instructions, so the kernel streams K and V at HBM speed where the scalar
+// kernel above is bound by its instruction issue.
+//
+// Warp roles (352 threads):
+//   warps 0-3  softmax: thread t owns key t of a tile (TMEM lane t of S^T) and
+//              dim t of O^T; then the epilogue and the merge of the splits
+//   warps 4-7  correction of remote K tiles (rows 16 apart per thread)
+//   warp 8     TMA producer of the K ring
+//   warp 9     TMA producer of the V ring
+//   warp 10    TMEM allocator and single-thread MMA issuer
+// TMEM (128 columns): S^T of tile v at 32 (v % 2) (the tile's own view) and
+// 32 (v % 2) + 16 (the exact view of the edge tile), O^T at 64.
+constexpr int kTcKeys = 128;
+constexpr int kTcNS = 3;
+constexpr int kTcThreads = 352;
+constexpr int kTcN = 16;
+constexpr float kTcRescaleThreshold = 8.0f;  // log2 units, as the prefill's lazy offset
+// Shorter caches take the scalar kernel: its fp32 P keeps outputs over a few
+// keys within the stated bounds, where the rounding of P to bf16 for the
+// tensor core is not averaged out.
+constexpr int kTcMinKeys = 256;
+
+struct TcCfg {
+    static constexpr int D = 128;
+    static constexpr int TILE = kTcKeys * D * 2;     // one K or V tile: 32 KB
+    static constexpr int REGION = kTcKeys * 64 * 2;  // one 64-column box of it: 16 KB
+    static constexpr int QBOX = kTcN * 128;          // 16 rows x 64 16-bit values: 2 KB
+    static constexpr int OPND = 2 * QBOX;            // a 16 x 128 operand (Q^T or P^T): 4 KB
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = OFF_K + kTcNS * TILE;
+    static constexpr int OFF_QE = OFF_V + kTcNS * TILE;  // exact q, bf16
+    static constexpr int OFF_QR = OFF_QE + OPND;         // corrected q, fp16
+    static constexpr int OFF_P = OFF_QR + OPND;          // P^T, two buffers
+    static constexpr int OFF_RED = OFF_P + 2 * OPND;     // fp32 [2][4 warps][8 heads] maxima, [4][16] sums
+    static constexpr int OFF_BAR = OFF_RED + (2 * 4 * 8 + 4 * 16) * 4;
+    static constexpr int B_KFULL = 0, B_KEMPTY = B_KFULL + kTcNS, B_KREADY = B_KEMPTY + kTcNS,
+                         B_VFULL = B_KREADY + kTcNS, B_VEMPTY = B_VFULL + kTcNS, B_SFULL = B_VEMPTY + kTcNS,
+                         B_PFULL = B_SFULL + 2, B_ODONE = B_PFULL + 2, B_QREADY = B_ODONE + 1,
+                         B_BANDQK = B_QREADY + 1, B_DRAIN = B_BANDQK + 1, NBAR = B_DRAIN + 1;
+    static constexpr int OFF_TMEM_SLOT = NBAR * 8, OFF_ABORT = OFF_TMEM_SLOT + 4, OFF_LAST = OFF_ABORT + 4;
+    static constexpr int SMEM = OFF_BAR + OFF_LAST + 4 + 1024;  // + alignment slack
+    static_assert(SMEM <= 232448, "shared memory budget");
+    // the merge's scratch (GRP x 256 weights, then m and l) reuses the K ring
+    static_assert(8 * 256 * 4 + 2 * 8 * 4 <= kTcNS * TILE, "merge scratch");
+};
+
+__device__ __forceinline__ uint32_t tc_opnd_off(int row, int col)
+{
+    // byte offset of 16-bit element (row, col) of a 16 x 128 K-major operand
+    // stored as two 128-byte-swizzled boxes of 64 columns
+    return (uint32_t)((col >> 6) * TcCfg::QBOX + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4) +
+                      (col & 7) * 2);
+}
+
+template <int GRP>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                     const DecodeArgs a, const __grid_constant__ jl::PhaseTable pt,
+                     const __grid_constant__ RotConsts rc)
+{
+    using C = TcCfg;
+    constexpr int D = C::D, NS = kTcNS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~(uintptr_t)1023);
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sQE = sbase + C::OFF_QE,
+                   sQR = sbase + C::OFF_QR, sP = sbase + C::OFF_P;
+    auto bar = [&](int idx) -> uint32_t { return sbase + C::OFF_BAR + 8u * (uint32_t)idx; };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_BAR + C::OFF_TMEM_SLOT);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_BAR + C::OFF_ABORT);
+    volatile int &s_last = *reinterpret_cast<volatile int *>(smem + C::OFF_BAR + C::OFF_LAST);
+    float *red = reinterpret_cast<float *>(smem + C::OFF_RED);
+    const WaitCtx wc{a.status, abort_flag};
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int hk = blockIdx.y, b = blockIdx.z, split = blockIdx.x;
+    const int n = a.n, g = a.g, ns = a.splits;
+    const int j_begin = split * a.chunk;
+    const int j_end = min(n, j_begin + a.chunk);
+    const int T = (j_end - j_begin + kTcKeys - 1) / kTcKeys;
+    const int j_split = (g > 1) ? max(0, n - a.w) : 0;  // keys below are remote
+    const bool any_remote = j_begin < j_split;
+    // tile classes: 0 exact, 1 remote, 2 crossed by the window edge
+    auto tclass = [&](int v) -> int {
+        const int j0 = j_begin + v * kTcKeys;
+        return j0 >= j_split ? 0 : (j0 + kTcKeys <= j_split ? 1 : 2);
+    };
+
+    if (tid == 0) {
+        for (int s = 0; s < NS; s++) {
+            mbar_init(bar(C::B_KFULL + s), 1);
+            mbar_init(bar(C::B_KEMPTY + s), 1);
+            mbar_init(bar(C::B_KREADY + s), 4);  // one per correction warp
+            mbar_init(bar(C::B_VFULL + s), 1);
+            mbar_init(bar(C::B_VEMPTY + s), 1);
+        }
+        for (int s = 0; s < 2; s++) {
+            mbar_init(bar(C::B_SFULL + s), 1);
+            mbar_init(bar(C::B_PFULL + s), 4);  // one per softmax warp
+        }
+        mbar_init(bar(C::B_ODONE), 1);
+        mbar_init(bar(C::B_QREADY), 4);
+        mbar_init(bar(C::B_BANDQK), 1);
+        mbar_init(bar(C::B_DRAIN), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 10) {
+        tmem_alloc(smem_u32(tmem_slot), 128);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const size_t hq0 = (size_t)b * a.Hq + (size_t)hk * GRP;
+    bool ok = true;
+    float m_run[GRP], l_run[GRP], lr_run[GRP];  // softmax state (warps 0-3)
+
+    if (warp == 8 || warp == 9) {
+        // ------------------------------------------------------------ producers: K (warp 8), V (warp 9)
+        if (lane == 0) {
+            const bool is_k = warp == 8;
+            const CUtensorMap *m = is_k ? &tk : &tv;
+            const uint32_t ring = is_k ? sK : sV;
+            const int b_full = is_k ? C::B_KFULL : C::B_VFULL, b_empty = is_k ? C::B_KEMPTY : C::B_VEMPTY;
+            prefetch_tmap(m);
+            int issued = 0;
+            for (int v = 0; v < T; v++) {
+                const int s = v % NS;
+                if (!(ok = wait_bar(bar(b_empty + s), ((v / NS) & 1) ^ 1, wc))) break;
+                mbar_arrive_expect_tx(bar(b_full + s), C::TILE);
+#pragma unroll
+                for (int r = 0; r < 2; r++)
+                    tma_load_4d(ring + s * C::TILE + r * C::REGION, m, bar(b_full + s), r * 64, hk,
+                                j_begin + v * kTcKeys, b);
+                issued = v + 1;
+            }
+            if (!ok)
+                for (int v = issued - NS < 0 ? 0 : issued - NS; v < issued; v++)
+                    drain_bar(bar(b_full + v % NS), (v / NS) & 1);
+        }
+    } else if (warp == 10) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idE = idesc_bf16_f32(128, kTcN, false, false);
+            constexpr uint32_t idR = idesc_f16_f32(128, kTcN, false, false);
+            constexpr uint32_t idPV = idesc_bf16_f32(128, kTcN, true, false);  // A = V^T, MN-major
+            auto qk = [&](int v, int group, uint32_t qaddr, uint32_t id) {
+                const uint64_t dk = sdesc_sw128(sK + (v % NS) * C::TILE, 16, 1024);
+                const uint64_t dq = sdesc_sw128(qaddr, 16, 1024);
+#pragma unroll
+                for (int k = 0; k < D / 16; k++)
+                    mma_f16_ss(tmem + 32u * (v & 1) + 16u * group,
+                               dk + (uint64_t)(((k >> 2) * C::REGION + (k & 3) * 32) >> 4),
+                               dq + (uint64_t)(((k >> 2) * C::QBOX + (k & 3) * 32) >> 4), id, k > 0 ? 1u : 0u);
+            };
+            // S^T(v): the edge tile's exact scores first, on the raw tile
+            auto qk_tile = [&](int v) -> bool {
+                const int s = v % NS, cls = tclass(v);
+                if (cls == 2) {
+                    if (!wait_bar(bar(C::B_KFULL + s), (v / NS) & 1, wc)) return false;
+                    tc_fence_after();
+                    qk(v, 1, sQE, idE);
+                    mma_commit(bar(C::B_BANDQK));
+                }
+                if (!wait_bar(bar(C::B_KREADY + s), (v / NS) & 1, wc)) return false;
+                tc_fence_after();
+                if (cls == 0) qk(v, 0, sQE, idE);
+                else qk(v, 0, sQR, idR);
+                mma_commit(bar(C::B_SFULL + (v & 1)));
+                mma_commit(bar(C::B_KEMPTY + s));
+                return true;
+            };
+            ok = wait_bar(bar(C::B_QREADY), 0, wc);
+            tc_fence_after();
+            if (ok) ok = qk_tile(0);
+            for (int v = 0; ok && v < T; v++) {
+                // QK of the next tile goes first: its softmax overlaps this P.V
+                if (v + 1 < T && !(ok = qk_tile(v + 1))) break;
+                const int s = v % NS;
+                if (!(ok = wait_bar(bar(C::B_PFULL + (v & 1)), (v >> 1) & 1, wc))) break;
+                if (!(ok = wait_bar(bar(C::B_VFULL + s), (v / NS) & 1, wc))) break;
+                tc_fence_after();
+                const uint64_t dv = sdesc_sw128(sV + s * C::TILE, C::REGION, 1024);
+                const uint64_t dp = sdesc_sw128(sP + (v & 1) * C::OPND, 16, 1024);
+#pragma unroll
+                for (int k = 0; k < kTcKeys / 16; k++)
+                    mma_f16_ss(tmem + 64u, dv + (uint64_t)((k * 2048) >> 4),
+                               dp + (uint64_t)(((k >> 2) * C::QBOX + (k & 3) * 32) >> 4), idPV,
+                               (v > 0 || k > 0) ? 1u : 0u);
+                mma_commit(bar(C::B_VEMPTY + s));
+                mma_commit(bar(C::B_ODONE));
+            }
+            if (!ok) {
+                // no MMA may still run when TMEM is released
+                mma_commit(bar(C::B_DRAIN));
+                drain_bar(bar(C::B_DRAIN), 0);
+            }
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ correction
+        // Makes K(v) ready for its QK: rotates a tile with remote keys in place
+        // (the edge tile after its exact QK has read it) and arrives on KREADY.
+        const int t = tid - 128;
+        Corrector<D> cor;
+        if (any_remote) cor.init(t, g, pt, rc);
+        for (int v = 0; ok && v < T; v++) {
+            const int s = v % NS, cls = tclass(v);
+            if (!(ok = wait_bar_warp(bar(C::B_KFULL + s), (v / NS) & 1, wc))) break;
+            if (cls == 2 && !(ok = wait_bar_warp(bar(C::B_BANDQK), 0, wc))) break;
+            if (cls != 0) {
+                cor.run_k(sK + s * C::TILE, (j_begin + v * kTcKeys) / kTcKeys);
+                fence_proxy_async_smem();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::B_KREADY + s));
+        }
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int t = tid;
+        const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+        const __nv_bfloat16 *qb = a.q + hq0 * D;
+        // Q^T operands: rows h < GRP hold the heads, the rest zero
+        for (int e = t; e < kTcN * 16; e += 128) {
+            const int h = e >> 4, cc = e & 15;
+            uint4 x = make_uint4(0u, 0u, 0u, 0u);
+            if (h < GRP) x = *reinterpret_cast<const uint4 *>(qb + h * D + cc * 8);
+            *reinterpret_cast<uint4 *>(smem + C::OFF_QE + tc_opnd_off(h, cc * 8)) = x;
+        }
+        if (any_remote) {
+            // corrected query at offset delta_{n-1} + qshift, fp16
+            const int di = jl::delta_pos(n - 1, g) + a.qshift;
+            for (int e = t; e < kTcN * 8; e += 128) {
+                const int h = e >> 3, cc = e & 7;
+                uint32_t lo[4] = {0u, 0u, 0u, 0u}, hi[4] = {0u, 0u, 0u, 0u};
+                if (h < GRP) {
+                    const uint4 x4 = *reinterpret_cast<const uint4 *>(qb + h * D + cc * 8);
+                    const uint4 y4 = *reinterpret_cast<const uint4 *>(qb + h * D + 64 + cc * 8);
+                    const uint32_t xw[4] = {x4.x, x4.y, x4.z, x4.w}, yw[4] = {y4.x, y4.y, y4.z, y4.w};
+#pragma unroll
+                    for (int e2 = 0; e2 < 4; e2++) {
+                        float xs[2], ys[2], xo[2], yo[2];
+                        jl::f2_split(jl::bf16x2_to_f2(xw[e2]), xs[0], xs[1]);
+                        jl::f2_split(jl::bf16x2_to_f2(yw[e2]), ys[0], ys[1]);
+#pragma unroll
+                        for (int u = 0; u < 2; u++) {
+                            float sn, cs;
+                            jl::phase_sincos(di, pt.f[cc * 8 + 2 * e2 + u], &sn, &cs);
+                            xo[u] = xs[u] * cs - ys[u] * sn;
+                            yo[u] = ys[u] * cs + xs[u] * sn;
+                        }
+                        lo[e2] = jl::f2_to_f16x2(jl::f2(xo[0], xo[1]));
+                        hi[e2] = jl::f2_to_f16x2(jl::f2(yo[0], yo[1]));
+                    }
+                }
+                *reinterpret_cast<uint4 *>(smem + C::OFF_QR + tc_opnd_off(h, cc * 8)) =
+                    make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                *reinterpret_cast<uint4 *>(smem + C::OFF_QR + tc_opnd_off(h, 64 + cc * 8)) =
+                    make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::B_QREADY));
+
+#pragma unroll
+        for (int h = 0; h < GRP; h++) {
+            m_run[h] = -INFINITY;
+            l_run[h] = 0.f;
+            lr_run[h] = 0.f;
+        }
+        const float sc = a.scale_log2;
+        for (int v = 0; v < T; v++) {
+            const int j = j_begin + v * kTcKeys + t;
+            const int cls = tclass(v);
+            const bool got = wait_bar_warp(bar(C::B_SFULL + (v & 1)), (v >> 1) & 1, wc);
+            float x[GRP], mx[GRP];
+            float *rm = red + (v & 1) * 32;
+            if (got) {
+                tc_fence_after();
+                uint32_t sa[16], sb[16];
+                tmem_ld16(tmem + lane_base + 32u * (v & 1), sa);
+                if (cls == 2) tmem_ld16(tmem + lane_base + 32u * (v & 1) + 16u, sb);
+                tmem_ld_wait();
+                const bool valid = j < j_end;
+                const bool exact_b = cls == 2 && j >= j_split;
+#pragma unroll
+                for (int h = 0; h < GRP; h++) {
+                    const float raw = __uint_as_float(exact_b ? sb[h] : sa[h]);
+                    x[h] = valid ? raw * sc : -INFINITY;
+                    mx[h] = x[h];
+                }
+                // the tile's maximum per head over the 128 keys
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                    for (int h = 0; h < GRP; h++) mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], o));
+                if (lane == 0)
+#pragma unroll
+                    for (int h = 0; h < GRP; h++) rm[warp * 8 + h] = mx[h];
+            }
+            if (!(ok = compute_sync_and(got))) break;
+            // Lazy offset (as in the prefill): moved only when the maximum grows
+            // by more than the threshold, by an integer, so rescaling is by an
+            // exact power of two.  Every thread takes the same decision.
+            float f[GRP];
+            bool moved = false;
+#pragma unroll
+            for (int h = 0; h < GRP; h++) {
+                const float tm = fmaxf(fmaxf(rm[h], rm[8 + h]), fmaxf(rm[16 + h], rm[24 + h]));
+                f[h] = 1.f;
+                if (tm > m_run[h] + kTcRescaleThreshold) {
+                    if (m_run[h] == -INFINITY) {
+                        m_run[h] = tm;  // no key of this head so far carried weight
+                    } else {
+                        const float k = ceilf(tm - m_run[h]);
+                        m_run[h] += k;
+                        f[h] = k >= 150.f ? 0.f : ldexpf(1.f, -(int)k);
+                        l_run[h] *= f[h];
+                        lr_run[h] *= f[h];
+                        moved = true;
+                    }
+                }
+            }
+            if (moved && v > 0) {
+                // O^T holds P.V of tiles < v once the P.V of tile v-1 completed
+                // (SFULL(v) implies P.V(v-2) complete, so ODONE is at most
+                // one phase behind and the parity wait is unambiguous)
+                const bool done = wait_bar_warp(bar(C::B_ODONE), (v - 1) & 1, wc);
+                if (!(ok = compute_sync_and(done))) break;
+                tc_fence_after();
+                uint32_t o[16];
+                tmem_ld16(tmem + lane_base + 64u, o);
+                tmem_ld_wait();
+#pragma unroll
+                for (int h = 0; h < GRP; h++) o[h] = __float_as_uint(__uint_as_float(o[h]) * f[h]);
+                tmem_st16(tmem + lane_base + 64u, o);
+                tmem_st_wait();
+            }
+            // P^T(v): its buffer was last read by the P.V of tile v-2, which
+            // completed before QK(v) (one issuing thread, in-order pipe)
+            uint8_t *pbuf = smem + C::OFF_P + (v & 1) * C::OPND;
+#pragma unroll
+            for (int h = 0; h < GRP; h++) {
+                const float off = (m_run[h] == -INFINITY) ? 0.f : m_run[h];
+                const float pv = exp2f(x[h] - off);
+                const __nv_bfloat16 pb = __float2bfloat16_rn(pv);
+                l_run[h] += pv;
+                lr_run[h] += __bfloat162float(pb);
+                *reinterpret_cast<__nv_bfloat16 *>(pbuf + tc_opnd_off(h, t)) = pb;
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::B_PFULL + (v & 1)));
+        }
+        // ------------------------------------------------------------ epilogue (TMEM part)
+        // The P.V of the last two tiles may both be in flight here (QK(T-1)
+        // was issued before P.V(T-2)), so ODONE can be two phases behind and
+        // a parity wait on the last phase alone would pass on the older one:
+        // wait for tile T-2's phase first.
+        if (ok && T >= 2) ok = compute_sync_and(wait_bar_warp(bar(C::B_ODONE), (T - 2) & 1, wc));
+        if (ok) ok = compute_sync_and(wait_bar_warp(bar(C::B_ODONE), (T - 1) & 1, wc));
+        float o_h[GRP];
+        if (ok) {
+            tc_fence_after();
+            uint32_t o[16];
+            tmem_ld16(tmem + lane_base + 64u, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int h = 0; h < GRP; h++) o_h[h] = __uint_as_float(o[h]);
+            // row sums over the 128 keys of every tile: per-thread parts -> totals
+#pragma unroll
+            for (int o2 = 16; o2 > 0; o2 >>= 1)
+#pragma unroll
+                for (int h = 0; h < GRP; h++) {
+                    l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], o2);
+                    lr_run[h] += __shfl_xor_sync(0xffffffffu, lr_run[h], o2);
+                }
+            float *rs = red + 64;
+            if (lane == 0)
+#pragma unroll
+                for (int h = 0; h < GRP; h++) {
+                    rs[warp * 16 + h] = l_run[h];
+                    rs[warp * 16 + 8 + h] = lr_run[h];
+                }
+            compute_sync();
+#pragma unroll
+            for (int h = 0; h < GRP; h++) {
+                l_run[h] = (rs[h] + rs[16 + h]) + (rs[32 + h] + rs[48 + h]);
+                lr_run[h] = (rs[8 + h] + rs[24 + h]) + (rs[40 + h] + rs[56 + h]);
+            }
+            if (t == 0)
+#pragma unroll
+                for (int h = 0; h < GRP; h++)
+                    // an infinite or NaN score (an input or corrected operand out of range)
+                    if (!(l_run[h] < INFINITY)) jl::record_status(a.status, JL_ERR_GUARD);
+            if (ns == 1) {
+#pragma unroll
+                for (int h = 0; h < GRP; h++) {
+                    a.out[(hq0 + h) * D + t] = __float2bfloat16_rn(o_h[h] / lr_run[h]);
+                    if (t == h) a.lse[hq0 + h] = (m_run[h] + log2f(l_run[h])) * kLn2;
+                }
+            } else {
+                // out is normalised by the sum of the rounded P that P.V used,
+                // lse by the fp32 sum; the merge weighs splits by l
+#pragma unroll
+                for (int h = 0; h < GRP; h++) {
+                    a.part_o[((hq0 + h) * ns + split) * D + t] = o_h[h] * (l_run[h] / lr_run[h]);
+                    if (t == h) {
+                        a.part_ml[((hq0 + h) * ns + split) * 2 + 0] = m_run[h];
+                        a.part_ml[((hq0 + h) * ns + split) * 2 + 1] = l_run[h];
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 10) tmem_dealloc(tmem, 128);
+    // the K ring is free now: the merge's scratch
+    if (warp < 4 && ok && ns > 1) {
+        float *mw = reinterpret_cast<float *>(smem + C::OFF_K);
+        ticket_and_merge<D, GRP>(a, b, hk, ns, ns, mw, mw + GRP * 256, mw + GRP * 256 + 8, s_last);
+    }
+}
+
+// Split plan: as many CTAs as the kernel keeps resident (two per SM up to four
+// heads per kv head, one above), at most 256 splits per (batch, kv head),
 // chunks a multiple of the 64-key block.  splits_cap bounds splits for every
 // n, and the workspace is sized by it, so one workspace serves every cache
 // length for the same (B, Hq, Hkv, D).
@@ -514,7 +1036,7 @@ struct Plan {
     int splits, chunk, splits_cap;
 };
 
-int resident_ctas(int) { return 2; }
+int resident_ctas(int grp) { return grp <= 4 ? DecOcc<4>::CTAS : DecOcc<8>::CTAS; }
 
 Plan make_plan(int B, int Hkv, int grp, int n)
 {
@@ -528,9 +1050,9 @@ Plan make_plan(int B, int Hkv, int grp, int n)
     return Plan{(int)splits, (int)chunk, (int)per_head};
 }
 
-// Paged batches mix lengths, so the split count is sized for the longest
-// sequence as if it alone filled the GPU (every resident CTA over its kv
-// heads); the splits of shorter sequences past their end exit at once.
+// Paged batches mix lengths: the grid gives every kv head splits_cap CTAs
+// (every resident CTA over the kv heads), which the kernel shares out among
+// the sequences in proportion to their lengths (it reads them on the device).
 Plan make_paged_plan(int Hkv, int grp, int max_n)
 {
     long long per_head = (148LL * resident_ctas(grp) + Hkv - 1) / Hkv;
@@ -561,10 +1083,12 @@ struct HostCache {
     int D = 0, g = 0;
     double theta = 0.0;
     jl::PhaseTable pt;
-    DecRot rot;
+    DecRot rot;     // the scalar kernel's chain step
+    RotConsts rc;   // the tensor-core kernel's tile correction
 };
 
-bool host_tables(int D, double theta, int g, const jl::PhaseTable **pt, const DecRot **rot)
+bool host_tables(int D, double theta, int g, const jl::PhaseTable **pt, const DecRot **rot,
+                 const RotConsts **rc = nullptr)
 {
     thread_local HostCache hc;
     if (hc.D != D || hc.theta != theta || hc.g != g) {
@@ -577,13 +1101,48 @@ bool host_tables(int D, double theta, int g, const jl::PhaseTable **pt, const De
             jl::rotation_host(hc.pt, d, step, &hc.rot.c[d], &hc.rot.s[d]);
             hc.rot.ns[d] = -hc.rot.s[d];
         }
+        make_rot_consts(hc.pt, D, g, &hc.rc);
         hc.D = D;
         hc.theta = theta;
         hc.g = g;
     }
     *pt = &hc.pt;
     *rot = &hc.rot;
+    if (rc) *rc = &hc.rc;
     return true;
+}
+
+// Split plan of the tensor-core kernel: one CTA per SM (its rings take most
+// of the shared memory), a single wave of at most 148 CTAs, chunks a multiple
+// of the 128-key tile; never more splits than the scalar plan's capacity, so
+// the same workspace serves both.
+Plan make_tc_plan(int B, int Hkv, int n, int splits_cap)
+{
+    long long per_head = 148LL / ((long long)B * Hkv);
+    if (per_head < 1) per_head = 1;
+    if (per_head > splits_cap) per_head = splits_cap;
+    long long chunk = (n + per_head - 1) / per_head;
+    chunk = (chunk + kTcKeys - 1) / kTcKeys * kTcKeys;
+    const long long splits = (n + chunk - 1) / chunk;
+    return Plan{(int)splits, (int)chunk, splits_cap};
+}
+
+template <int GRP>
+int launch_tc(const DecodeArgs &a, int B, const CUtensorMap &tk, const CUtensorMap &tv,
+              const jl::PhaseTable &pt, const RotConsts &rc, cudaStream_t st)
+{
+    auto kern = decode_tc_kernel<GRP>;
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return jl::cuda_status(cudaGetLastError());
+    if (!attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg::SMEM);
+        if (e != cudaSuccess) return jl::cuda_status(e);
+        attr_set[dev] = true;
+    }
+    dim3 grid(a.splits, a.Hkv, B);
+    kern<<<grid, kTcThreads, TcCfg::SMEM, st>>>(tk, tv, a, pt, rc);
+    return jl::cuda_status(cudaGetLastError());
 }
 
 template <int D, int GRP, bool PAGED>
@@ -600,7 +1159,9 @@ int launch(const DecodeArgs &a, int B, const CUtensorMap &tk, const CUtensorMap 
         if (e != cudaSuccess) return jl::cuda_status(e);
         attr_set[dev] = true;
     }
-    dim3 grid(a.splits, a.Hkv, B);
+    // paged: a.splits CTAs per kv head shared by the batch in proportion to the
+    // lengths, plus one per sequence for rounding; the surplus exits at once
+    dim3 grid(PAGED ? a.splits + B : a.splits, a.Hkv, PAGED ? 1 : B);
     kern<<<grid, kThreads, C::SMEM, st>>>(tk, tv, a, pt, rot);
     return jl::cuda_status(cudaGetLastError());
 }
@@ -677,7 +1238,9 @@ int common_setup(DecodeArgs &a, const void *q, void *out, float *lse, int B, int
     a.n = n;
     a.w = w;
     a.L = L_pre;
-    a.splits = p.splits;
+    // paged: the CTA target per kv head (the device derives each sequence's
+    // share); otherwise this length's split count
+    a.splits = paged ? p.splits_cap : p.splits;
     a.chunk = p.chunk;
     a.scale_log2 = (float)(1.0 / sqrt((double)D) * 1.4426950408889634);
     return JL_OK;
@@ -711,8 +1274,24 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache, 
     a.qshift = qshift;
     const jl::PhaseTable *pt = nullptr;
     const DecRot *rot = nullptr;
-    if (!host_tables(D, theta, a.g, &pt, &rot)) return JL_ERR_ARG;
+    const RotConsts *rcs = nullptr;
+    if (!host_tables(D, theta, a.g, &pt, &rot, &rcs)) return JL_ERR_ARG;
     CUtensorMap tk, tv;
+    if (D == 128 && n >= kTcMinKeys) {
+        // the tensor-core kernel: 128-key tiles as two 64-column swizzled boxes
+        const Plan p = make_tc_plan(B, Hkv, n, make_plan(B, Hkv, Hq / Hkv, n).splits_cap);
+        a.splits = p.splits;
+        a.chunk = p.chunk;
+        if (!jl::make_bshd_map(&tk, k_cache, B, n, n_cap, Hkv, D, 64, kTcKeys, true) ||
+            !jl::make_bshd_map(&tv, v_cache, B, n, n_cap, Hkv, D, 64, kTcKeys, true))
+            return JL_ERR_CUDA;
+        switch (Hq / Hkv) {
+        case 1: return launch_tc<1>(a, B, tk, tv, *pt, *rcs, (cudaStream_t)stream);
+        case 2: return launch_tc<2>(a, B, tk, tv, *pt, *rcs, (cudaStream_t)stream);
+        case 4: return launch_tc<4>(a, B, tk, tv, *pt, *rcs, (cudaStream_t)stream);
+        default: return launch_tc<8>(a, B, tk, tv, *pt, *rcs, (cudaStream_t)stream);
+        }
+    }
     // only rows [0, n) are mapped: the block that holds key n-1 reads zeros past
     // it, never the cache's unused capacity (0 * NaN would poison P.V)
     if (!jl::make_bshd_map(&tk, k_cache, B, n, n_cap, Hkv, D, D, kKB, false) ||
@@ -786,6 +1365,7 @@ extern "C" int jl_bifocal_decode_paged(const void *q, const void *k_pages, const
     a.page_size = page_size;
     a.max_pages = max_pages;
     a.num_pages = num_pages;
+    a.B = B;
     const jl::PhaseTable *pt = nullptr;
     const DecRot *rot = nullptr;
     if (!host_tables(D, theta, 1, &pt, &rot)) return JL_ERR_ARG;  // per-sequence g on the device

@@ -41,6 +41,7 @@
 #include "jl_common.cuh"
 #include "sm100_ptx.cuh"
 #include "tile_class.cuh"
+#include "corrector.cuh"
 
 namespace {
 
@@ -95,259 +96,12 @@ struct Params {
     float scale_log2;    // tau * log2(e)
 };
 
-// Byte offset of 16-byte chunk `cc` of row `n` inside a 128-byte-swizzled box.
-__device__ __forceinline__ uint32_t sw128(int n, int cc)
-{
-    return (uint32_t)(n * 128 + ((cc ^ (n & 7)) << 4));
-}
-
 __device__ __forceinline__ float fast_exp2(float x)
 {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-
-// Unit rotations per rotation pair d, computed on the host from the exact
-// fixed-point phase, as cosine, sine and negated sine arrays (pairs of
-// consecutive d load as one f32x2): a = rotation by (RPS/g - RPS) * theta_d
-// (RPS rows further, no group boundary crossed), b = by (RPS/g + 1 - RPS) *
-// theta_d (one boundary crossed), a2 = by twice a.
-struct RotConsts {
-    alignas(8) float ac[64];
-    alignas(8) float as[64];
-    alignas(8) float ans[64];
-    alignas(8) float bc[64];
-    alignas(8) float bs[64];
-    alignas(8) float bns[64];
-    alignas(8) float a2c[64];
-    alignas(8) float a2s[64];
-    alignas(8) float a2ns[64];
-    int uni;  // g divides RPS: every RPS-row step is a
-};
-
-// Rotates 128-row bf16 tiles (SW128 boxes) in place by delta_p, p = p0 + row,
-// writing fp16: the corrected operands feed a kind::f16 MMA with fp16 A and
-// B, whose 11-bit significand keeps the rounding of the aliased view ~8x
-// below bf16's (the rotation preserves each pair's norm, so |x| < 46000
-// stays finite).  Thread t of the 128-thread group owns chunk pair
-// c = t % CPR (pairs d = 8c..8c+7) and rows n0 + RPS*k; the arithmetic runs
-// on packed fp32 pairs (two consecutive d per instruction).
-//
-// Angles.  When g divides RPS, delta moves by the same amount every RPS rows,
-// so two chains of unit complex numbers (even and odd steps of this thread's
-// rows, each advanced by a2) cover a tile with independent work, and after a
-// tile they have advanced exactly to the first rows of the next tile: the
-// remote K tiles come in order 0, 1, 2, ..., so the chains carry over and
-// are re-anchored from the exact phase only every kReanchorTiles tiles.
-// Otherwise every tile is anchored exactly and each step picks a or b.
-//
-// ROWS = 64 serves the pair kernel, whose CTAs hold one half of each K tile:
-// its chains then skip the other CTA's 64 rows after every tile.
-template <int D, int ROWS = 128>
-struct Corrector {
-    static constexpr int CPR = D / 16;        // chunk pairs per row
-    static constexpr int RPS = 128 / CPR;     // rows per step
-    static constexpr int STEPS = ROWS / RPS;  // rows per thread
-    static constexpr int kReanchorTiles = 32;
-    static constexpr uint32_t REGION = ROWS * 64 * 2;  // one 64-column box of the tile
-    int c, n0, g, next_kt;
-    bool uni;
-    const unsigned long long *F;  // this thread's 8 phases (parameter space)
-    const RotConsts *rc;
-    jl::f32x2 ec[4], es[4], oc[4], os[4];  // chains: rows n0 and n0 + RPS of tile next_kt
-
-    __device__ void init(int t, int g_, const jl::PhaseTable &pt, const RotConsts &rc_)
-    {
-        c = t % CPR;
-        n0 = t / CPR;
-        g = g_;
-        F = pt.f + 8 * c;
-        rc = &rc_;
-        uni = rc_.uni != 0;
-        next_kt = -1;
-    }
-
-    __device__ __forceinline__ void offsets(int n, uint32_t &lo, uint32_t &hi) const
-    {
-        lo = sw128(n, c);
-        hi = (D == 128) ? REGION + lo : sw128(n, c + 4);
-    }
-
-    __device__ __forceinline__ static jl::f32x2 ld2(const float *p)
-    {
-        return *reinterpret_cast<const jl::f32x2 *>(p);
-    }
-
-    // (x, y) -> (x c - y s, y c + x s) for 8 pairs, fp16 out
-    __device__ __forceinline__ static void rotate(const uint32_t (&a)[4], const uint32_t (&b)[4],
-                                                  const jl::f32x2 (&zc)[4], const jl::f32x2 (&zs)[4],
-                                                  uint32_t (&ao)[4], uint32_t (&bo)[4])
-    {
-#pragma unroll
-        for (int q = 0; q < 4; q++) {
-            const jl::f32x2 x = jl::bf16x2_to_f2(a[q]), y = jl::bf16x2_to_f2(b[q]);
-            const jl::f32x2 ny = y ^ 0x8000000080000000ull;
-            ao[q] = jl::f2_to_f16x2(jl::fma2(x, zc[q], jl::mul2(ny, zs[q])));
-            bo[q] = jl::f2_to_f16x2(jl::fma2(y, zc[q], jl::mul2(x, zs[q])));
-        }
-    }
-
-    // z <- z * (cos + i sin) for the 8 pairs, given cos / sin / -sin arrays
-    __device__ __forceinline__ static void cmul(jl::f32x2 (&zc)[4], jl::f32x2 (&zs)[4],
-                                                const jl::f32x2 (&rcs)[4], const jl::f32x2 (&rsn)[4],
-                                                const jl::f32x2 (&rns)[4])
-    {
-#pragma unroll
-        for (int q = 0; q < 4; q++) {
-            const jl::f32x2 nc = jl::fma2(zc[q], rcs[q], jl::mul2(zs[q], rns[q]));
-            const jl::f32x2 ns = jl::fma2(zs[q], rcs[q], jl::mul2(zc[q], rsn[q]));
-            zc[q] = nc;
-            zs[q] = ns;
-        }
-    }
-
-    __device__ __forceinline__ static void ld4(uint32_t addr, uint32_t (&r)[4])
-    {
-        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                     : "r"(addr));
-    }
-
-    __device__ __forceinline__ static void st4(uint32_t addr, const uint32_t (&r)[4])
-    {
-        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(r[0]), "r"(r[1]),
-                     "r"(r[2]), "r"(r[3])
-                     : "memory");
-    }
-
-    __device__ void sincos8(int off, jl::f32x2 (&zc)[4], jl::f32x2 (&zs)[4]) const
-    {
-#pragma unroll
-        for (int q = 0; q < 4; q++) {
-            float s0, c0, s1, c1;
-            jl::phase_sincos(off, F[2 * q], &s0, &c0);
-            jl::phase_sincos(off, F[2 * q + 1], &s1, &c1);
-            zc[q] = jl::f2(c0, c1);
-            zs[q] = jl::f2(s0, s1);
-        }
-    }
-
-    // exact anchors of both chains at rows p and p + RPS (offsets delta + off)
-    __device__ void anchor(int p, int off = 0)
-    {
-        sincos8(jl::delta_pos(p, g) + off, ec, es);
-        sincos8(jl::delta_pos(p + RPS, g) + off, oc, os);
-    }
-
-    // g divides RPS: rows n0 + 2k*RPS on the even chain, n0 + (2k+1)*RPS on
-    // the odd one, both advanced by a2 after every pair of rows
-    __device__ void run_uni(uint32_t tile)
-    {
-        jl::f32x2 rcs[4], rsn[4], rns[4];
-#pragma unroll
-        for (int q = 0; q < 4; q++) {
-            rcs[q] = ld2(rc->a2c + 8 * c + 2 * q);
-            rsn[q] = ld2(rc->a2s + 8 * c + 2 * q);
-            rns[q] = ld2(rc->a2ns + 8 * c + 2 * q);
-        }
-#pragma unroll 1
-        for (int k = 0; k < STEPS / 2; k++) {
-            const int ne = n0 + 2 * k * RPS, no = ne + RPS;
-            uint32_t le, he, lo_, ho;
-            offsets(ne, le, he);
-            offsets(no, lo_, ho);
-            uint32_t a0[4], b0[4], a1[4], b1[4], r0[4], q0[4], r1[4], q1[4];
-            ld4(tile + le, a0);
-            ld4(tile + he, b0);
-            ld4(tile + lo_, a1);
-            ld4(tile + ho, b1);
-            rotate(a0, b0, ec, es, r0, q0);
-            rotate(a1, b1, oc, os, r1, q1);
-            st4(tile + le, r0);
-            st4(tile + he, q0);
-            st4(tile + lo_, r1);
-            st4(tile + ho, q1);
-            cmul(ec, es, rcs, rsn, rns);
-            cmul(oc, os, rcs, rsn, rns);
-        }
-    }
-
-    // any g: exact anchor at row n0, then per RPS rows a or b
-    __device__ void run_generic(uint32_t tile, int p0, int off = 0) const
-    {
-        jl::f32x2 zc[4], zs[4];
-        const int p = p0 + n0;
-        sincos8(jl::delta_pos(p, g) + off, zc, zs);
-        const int rs = RPS % g;
-        int jm = p % g;
-#pragma unroll 1
-        for (int k = 0; k < STEPS; k++) {
-            uint32_t lo_, hi_;
-            offsets(n0 + RPS * k, lo_, hi_);
-            uint32_t a[4], b[4], ao[4], bo[4];
-            ld4(tile + lo_, a);
-            ld4(tile + hi_, b);
-            rotate(a, b, zc, zs, ao, bo);
-            st4(tile + lo_, ao);
-            st4(tile + hi_, bo);
-            jm += rs;
-            const bool carry = jm >= g;
-            if (carry) jm -= g;
-            jl::f32x2 rcs[4], rsn[4], rns[4];
-#pragma unroll
-            for (int q = 0; q < 4; q++) {
-                const int i = 8 * c + 2 * q;
-                rcs[q] = ld2(carry ? rc->bc + i : rc->ac + i);
-                rsn[q] = ld2(carry ? rc->bs + i : rc->as + i);
-                rns[q] = ld2(carry ? rc->bns + i : rc->ans + i);
-            }
-            cmul(zc, zs, rcs, rsn, rns);
-        }
-    }
-
-    // the query tile at rows p0..p0+127, offsets delta + qshift (leaves the K
-    // chains to be re-anchored)
-    __device__ void run_q(uint32_t tile, int p0, int qshift)
-    {
-        if (uni) {
-            anchor(p0 + n0, qshift);
-            run_uni(tile);
-            next_kt = -1;
-        } else {
-            run_generic(tile, p0, qshift);
-        }
-    }
-
-    // remote K tile kt (tiles arrive in increasing order); row0 = position of
-    // the held rows' first row within the 128-key tile (0, or 64 for the
-    // second half in the pair kernel)
-    __device__ void run_k(uint32_t tile, int kt, int row0 = 0)
-    {
-        if (uni) {
-            if (kt != next_kt || kt % kReanchorTiles == 0) anchor(kt * kBN + row0 + n0);
-            run_uni(tile);
-            if (ROWS < kBN) {
-                // skip the rows the other CTA holds: the chains step 2 RPS rows per a2
-                jl::f32x2 rcs[4], rsn[4], rns[4];
-#pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    rcs[q] = ld2(rc->a2c + 8 * c + 2 * q);
-                    rsn[q] = ld2(rc->a2s + 8 * c + 2 * q);
-                    rns[q] = ld2(rc->a2ns + 8 * c + 2 * q);
-                }
-#pragma unroll 1
-                for (int k = 0; k < (kBN - ROWS) / (2 * RPS); k++) {
-                    cmul(ec, es, rcs, rsn, rns);
-                    cmul(oc, os, rcs, rsn, rns);
-                }
-            }
-            next_kt = kt + 1;
-        } else {
-            run_generic(tile, kt * kBN + row0);
-        }
-    }
-};
 
 // The virtual-tile sequence of one query tile (identical in every role).
 // Key-tile classes are monotone in the key tile index kt: remote, then band
@@ -1280,18 +1034,38 @@ __global__ void __launch_bounds__(kFewThreads)
     for (int j = t; j <= i; j += kFewThreads) {
         const __nv_bfloat16 *kj = a.k + (((size_t)b * a.n_cap + j) * a.Hkv + hk) * D;
         float acc = 0.f;
+        const uint4 *k16 = reinterpret_cast<const uint4 *>(kj);  // 8 bf16 per 16-byte load
         if (i - j < a.w || (a.g == 1 && !a.sliding)) {
-            for (int d = 0; d < D; d++) acc = fmaf(sq[d], __bfloat162float(kj[d]), acc);
+            float acc2 = 0.f;
+#pragma unroll 4
+            for (int c8 = 0; c8 < D / 8; c8++) {
+                const uint4 u = k16[c8];
+                const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    acc = fmaf(sq[8 * c8 + 2 * e], jl::bf16lo(w4[e]), acc);
+                    acc2 = fmaf(sq[8 * c8 + 2 * e + 1], jl::bf16hi(w4[e]), acc2);
+                }
+            }
+            acc += acc2;
         } else if (a.sliding) {
             acc = -INFINITY;  // outside a sliding window: not attended
         } else {
             const int dj = jl::delta_pos(j, a.g);
-            for (int d = 0; d < HALF; d++) {
-                float sn, cs;
-                jl::phase_sincos(dj, pt.f[d], &sn, &cs);
-                const float x = __bfloat162float(kj[d]), y = __bfloat162float(kj[d + HALF]);
-                acc = fmaf(sqg[d], x * cs - y * sn, acc);
-                acc = fmaf(sqg[d + HALF], y * cs + x * sn, acc);
+#pragma unroll 1
+            for (int c8 = 0; c8 < HALF / 8; c8++) {
+                const uint4 ul = k16[c8], uh = k16[HALF / 8 + c8];
+                const uint32_t lo4[4] = {ul.x, ul.y, ul.z, ul.w}, hi4[4] = {uh.x, uh.y, uh.z, uh.w};
+#pragma unroll
+                for (int e = 0; e < 8; e++) {
+                    const int d = 8 * c8 + e;
+                    float sn, cs;
+                    jl::phase_sincos(dj, pt.f[d], &sn, &cs);
+                    const float x = (e & 1) ? jl::bf16hi(lo4[e / 2]) : jl::bf16lo(lo4[e / 2]);
+                    const float y = (e & 1) ? jl::bf16hi(hi4[e / 2]) : jl::bf16lo(hi4[e / 2]);
+                    acc = fmaf(sqg[d], x * cs - y * sn, acc);
+                    acc = fmaf(sqg[d + HALF], y * cs + x * sn, acc);
+                }
             }
         }
         sc[j] = acc * a.scale_log2;
@@ -1323,10 +1097,16 @@ __global__ void __launch_bounds__(kFewThreads)
     for (int q = 0; q < kFewThreads / 32; q++) l += red[q];
     const float inv_l = 1.f / l;
     for (int d = t; d < D; d += kFewThreads) {
-        float o = 0.f;
-        for (int j = 0; j <= i; j++)
-            o = fmaf(sc[j], __bfloat162float(a.v[(((size_t)b * a.n_cap + j) * a.Hkv + hk) * D + d]), o);
-        a.out[qrow * D + d] = __float2bfloat16_rn(o * inv_l);
+        const __nv_bfloat16 *vd = a.v + ((size_t)b * a.n_cap * a.Hkv + hk) * D + d;
+        const size_t vs = (size_t)a.Hkv * D;  // one key further
+        float o[4] = {0.f, 0.f, 0.f, 0.f};
+        int j = 0;
+        for (; j + 3 <= i; j += 4) {
+#pragma unroll
+            for (int u = 0; u < 4; u++) o[u] = fmaf(sc[j + u], __bfloat162float(vd[(j + u) * vs]), o[u]);
+        }
+        for (; j <= i; j++) o[0] = fmaf(sc[j], __bfloat162float(vd[j * vs]), o[0]);
+        a.out[qrow * D + d] = __float2bfloat16_rn(((o[0] + o[1]) + (o[2] + o[3])) * inv_l);
     }
     if (t == 0) a.lse[((size_t)b * a.Hq + h) * a.lse_stride + (i - a.pos0)] = (m + log2f(l)) * kLn2;
 }
@@ -1398,18 +1178,7 @@ static int prefill_rows(const PrefillCall &c, const void *q, void *out, float *l
     p.scale_log2 = c.scale_log2;
     // step rotations of the correction (rows per step: 16 at D = 128, 32 at D = 64)
     RotConsts rc;
-    memset(&rc, 0, sizeof(rc));
-    const int rps = 128 / (D / 16);
-    const long long qs = rps / g;
-    rc.uni = (rps % g == 0) ? 1 : 0;
-    for (int d = 0; d < D / 2; d++) {
-        jl::rotation_host(c.pt, d, qs - rps, &rc.ac[d], &rc.as[d]);
-        jl::rotation_host(c.pt, d, qs + 1 - rps, &rc.bc[d], &rc.bs[d]);
-        jl::rotation_host(c.pt, d, 2 * (qs - rps), &rc.a2c[d], &rc.a2s[d]);
-        rc.ans[d] = -rc.as[d];
-        rc.bns[d] = -rc.bs[d];
-        rc.a2ns[d] = -rc.a2s[d];
-    }
+    make_rot_consts(c.pt, D, g, &rc);
     int rc_launch;
     if (c.pair && D == 128 && p.grp % 4 == 0) {
         // four heads per kv head or a multiple: a CTA pair per query tile of four heads
