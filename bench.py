@@ -36,23 +36,33 @@ WORKLOAD = dict(B=1, Hq=32, Hkv=8, D=128, S=131072, L_pre=32768, w=4096, theta=1
 DECODE_NS = (8192, 32768, 131072)
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 # DRAM bytes (read + write) of one 128K bifocal prefill launch, from the ncu
-# counters of a one-launch capture, valid only for the prefill source they were
-# measured on (first 16 hex digits of its sha256).
-PREFILL_TRAFFIC = {"sha256_16": "42ec6803786d95ff", "bytes": 3.554e9 + 1.058e9}
+# counters of a one-launch capture, valid only for the prefill sources they
+# were measured on (first 16 hex digits of the sha256 of their concatenation).
+PREFILL_TRAFFIC = {"sha256_16": "e9309379a4190452", "bytes": 3.5534e9 + 1.0576e9}
+PREFILL_SOURCES = ("prefill.cu", "corrector.cuh", "sm100_ptx.cuh", "jl_common.cuh", "tile_class.cuh")
+
+
+def prefill_sources_sha16():
+    import hashlib
+
+    h = hashlib.sha256()
+    for name in PREFILL_SOURCES:
+        with open(os.path.join(ROOT, "zero_shot_rope_02_b300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def prefill_traffic():
-    import hashlib
-
-    path = os.path.join(ROOT, "zero_shot_rope_02_b300", "csrc", "prefill.cu")
-    with open(path, "rb") as f:
-        h = hashlib.sha256(f.read()).hexdigest()[:16]
-    return PREFILL_TRAFFIC["bytes"] if h == PREFILL_TRAFFIC["sha256_16"] else None
+    return PREFILL_TRAFFIC["bytes"] if prefill_sources_sha16() == PREFILL_TRAFFIC["sha256_16"] else None
 
 
-def prefill_kernel_name(grp, D):
-    """The tile kernel libjetlong dispatches to by default: one CTA per query
-    tile of two heads of a GQA group (one when the group size is odd)."""
+def prefill_kernel_name(grp, D, remote=True):
+    """The tile kernel libjetlong dispatches a launch to by default: the two-SM
+    kernel at D = 128 with a multiple of four heads per kv head when the launch
+    has remote keys, else one CTA per query tile of two heads of a GQA group
+    (one when the group size is odd)."""
+    if remote and D == 128 and grp % 4 == 0:
+        return "prefill_pair_kernel"
     return f"prefill_kernel<{D},{2 if grp % 2 == 0 else 1}>"
 
 
@@ -219,9 +229,14 @@ def run_ours(args, rank, world, dev):
     if jl.jl_debug_status() != 0:
         raise RuntimeError("device status word set during the timed region")
 
-    # bifocal off: the same kernel with L_pre >= S (g = 1)
+    # bifocal off: L_pre >= S (g = 1), as the library runs it by default, and
+    # on the same tile kernel as the bifocal run
     plain_ms = time_calls(lambda: jl.jl_bifocal_prefill(q, k, v, S, w, theta, out=out, lse=lse,
                                                         stream=stream), stream, dev, reps=max(3, args.steps))
+    same_flags = jl.JL_PREFILL_CTA_PAIR if prefill_kernel_name(Hq // Hkv, D) == "prefill_pair_kernel" else \
+        jl.JL_PREFILL_ONE_CTA
+    plain_same_ms = time_calls(lambda: jl.jl_bifocal_prefill_ex(q, k, v, 0, S, w, theta, same_flags, out=out,
+                                                                lse=lse, stream=stream), stream, dev, reps=3)
     decode = decode_sweep(jl, dev, stream, peaks)
     # the method's optional forms on the same 128K layer (same FLOP convention)
     variants = {}
@@ -232,13 +247,14 @@ def run_ours(args, rank, world, dev):
         variants[name] = {"ms": round(v_ms, 3), "tflops_causal_convention": round(flops / (v_ms * 1e-3) / 1e12, 2),
                           "g": jl.jl_group_factor_ex(S, L, w, flags)}
     variants["sliding_window"]["note"] = "attends only the last w keys: FLOPs counted on the full causal convention"
-    # the two-SM tile kernel (cta_group::2), opt-in: bifocal and plain on the same layer
-    pair = {}
+    # the other tile kernel on the same layer (JL_PREFILL_ONE_CTA: one CTA per
+    # query tile of two heads), bifocal and plain
+    one_cta = {}
     for tag, L_pre in (("bifocal", L), ("plain", S)):
-        pair[tag + "_ms"] = round(time_calls(lambda Lp=L_pre: jl.jl_bifocal_prefill_ex(
-            q, k, v, 0, Lp, w, theta, jl.JL_PREFILL_CTA_PAIR, out=out, lse=lse, stream=stream), stream, dev, reps=3), 3)
-    pair["bifocal_overhead"] = round(pair["bifocal_ms"] / pair["plain_ms"] - 1.0, 4)
-    pair["tflops"] = round(flops / (pair["bifocal_ms"] * 1e-3) / 1e12, 2)
+        one_cta[tag + "_ms"] = round(time_calls(lambda Lp=L_pre: jl.jl_bifocal_prefill_ex(
+            q, k, v, 0, Lp, w, theta, jl.JL_PREFILL_ONE_CTA, out=out, lse=lse, stream=stream), stream, dev, reps=3), 3)
+    one_cta["bifocal_overhead"] = round(one_cta["bifocal_ms"] / one_cta["plain_ms"] - 1.0, 4)
+    one_cta["tflops"] = round(flops / (one_cta["bifocal_ms"] * 1e-3) / 1e12, 2)
     if jl.jl_debug_status() != 0:
         raise RuntimeError("device status word set by the variant runs")
     # chunked prefill: the last 8K tokens of the same context over the cache of
@@ -275,10 +291,13 @@ def run_ours(args, rank, world, dev):
         "prefill": {"tflops": round(achieved, 2), "ms": round(avg_prefill_ms, 3),
                     "frac_of_bf16_peak": round(achieved / peaks["bf16_tflops"], 4)},
         "plain_rope": {"tflops": round(flops / (plain_ms * 1e-3) / 1e12, 2), "ms": round(plain_ms, 3),
-                       "bifocal_overhead": round(avg_prefill_ms / plain_ms - 1.0, 4)},
+                       "kernel": prefill_kernel_name(Hq // Hkv, D, remote=False),
+                       "bifocal_overhead": round(avg_prefill_ms / plain_ms - 1.0, 4),
+                       "same_kernel_ms": round(plain_same_ms, 3),
+                       "same_kernel_overhead": round(avg_prefill_ms / plain_same_ms - 1.0, 4)},
         "decode": decode,
         "variants": variants,
-        "prefill_cta_pair": pair,
+        "prefill_one_cta": one_cta,
         "paged_decode": paged,
         "rope_cache_write": {"rows": S, "us": round(1e3 * cw_ms, 2),
                              "gbs": round(cw_bytes / (cw_ms * 1e-3) / 1e9, 1),
@@ -590,7 +609,7 @@ def run_case(args):
         lse = torch.empty((1, cfg["Hq"], args.S), dtype=torch.float32, device=dev)
         L = args.L if args.L > 0 else cfg["L_pre"]
 
-        flags = jl.JL_PREFILL_CTA_PAIR if args.pair else 0
+        flags = jl.JL_PREFILL_CTA_PAIR if args.pair else (jl.JL_PREFILL_ONE_CTA if args.one_cta else 0)
 
         def call():
             jl.jl_bifocal_prefill_ex(q, k, v, 0, L, cfg["w"], cfg["theta"], flags, out=out, lse=lse, stream=stream)
@@ -632,7 +651,9 @@ def main():
     ap.add_argument("--L", type=int, default=0)
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--pair", action="store_true",
-                    help="--case prefill: the two-SM tile kernel (JL_PREFILL_CTA_PAIR)")
+                    help="--case prefill: force the two-SM tile kernel (JL_PREFILL_CTA_PAIR)")
+    ap.add_argument("--one-cta", action="store_true",
+                    help="--case prefill: force the one-CTA tile kernel (JL_PREFILL_ONE_CTA)")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)

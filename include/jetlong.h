@@ -119,18 +119,24 @@ int jl_group_factor(int64_t s, int64_t L_pre, int32_t *g_out);
 #define JL_VARIANT_QUERY_SHIFT 4u
 
 /*
- * Kernel choice of jl_bifocal_prefill_ex (combines with the variant flags):
- * JL_PREFILL_CTA_PAIR runs, where it applies (D = 128 and Hq / Hkv a multiple
- * of 4), the two-SM tile kernel: a cluster of two CTAs per query tile of four
- * heads, tcgen05 MMAs of M = 256 across both SMs (cta_group::2), each CTA
- * loading and correcting half of every K tile.  It computes the same result
- * (parity-tested like the default) with half the correction work per SM, but
- * each tile's softmax -> MMA handshake then crosses SMs; on B300 it measured
- * 151 ms bifocal / 137 ms plain at the 128K Qwen3-8B-shaped layer against
- * 137 / 114 ms for the default one-CTA kernel, so it is not the default.
- * Elsewhere the flag is ignored.
+ * Kernel choice of jl_bifocal_prefill_ex (combines with the variant flags).
+ * Two tile kernels compute the same result (both parity-tested):
+ *   - the one-CTA kernel: a CTA per 128-row query tile of two heads that share
+ *     a kv head, every K tile it visits corrected by that CTA;
+ *   - the two-SM kernel, where it applies (D = 128 and Hq / Hkv a multiple of
+ *     4): a cluster of two CTAs per query tile of four heads, tcgen05 MMAs of
+ *     M = 256 across both SMs (cta_group::2), each CTA loading and correcting
+ *     half of every K tile -- half the correction work per SM.
+ * By default a launch takes the two-SM kernel where it applies and the launch
+ * has remote keys (g > 1, not a sliding-window layer, s - 1 >= w), the one-CTA
+ * kernel otherwise: at the 128K Qwen3-8B-shaped layer on B300 the two-SM
+ * kernel measured ~134 ms bifocal against ~137 ms, and ~116 ms plain against
+ * ~114 ms.  JL_PREFILL_CTA_PAIR forces the two-SM kernel wherever it applies
+ * (ignored elsewhere); JL_PREFILL_ONE_CTA forces the one-CTA kernel; both
+ * together are JL_ERR_ARG.
  */
 #define JL_PREFILL_CTA_PAIR 8u
+#define JL_PREFILL_ONE_CTA 16u
 
 /*
  * Group factor under variant flags -- host, pure.  Without JL_VARIANT_QUERY_SHIFT
@@ -238,7 +244,7 @@ int jl_bifocal_prefill_chunk(const void *q, const void *k_cache, const void *v_c
  * [(g-1) L_pre, g L_pre) -- each scored as the chunk of a prefill of length
  * g L_pre.  SLIDING visits only the key tiles the window reaches.
  * QUERY_SHIFT shifts the query's correction offset by w - floor(w/g).
- * JL_PREFILL_CTA_PAIR selects the two-SM tile kernel (see above).
+ * JL_PREFILL_CTA_PAIR / JL_PREFILL_ONE_CTA choose the tile kernel (see above).
  * Returns what jl_bifocal_prefill_chunk returns; JL_ERR_ARG also for an unknown
  * flag, SLIDING with another variant flag, or a QUERY_SHIFT with no valid g;
  * JL_ERR_UNSUPPORTED for PER_QUERY_G with QUERY_SHIFT.

@@ -108,7 +108,8 @@ def test_variant_entry_points_reject_bad_flags(jl):
         return jl.lib.jl_bifocal_decode_ex(GOOD, GOOD, GOOD, GOOD, GOOD, 1, 32, 8, n, n, 128, L, w, 1e6,
                                            flags, GOOD, 1 << 30, None)
 
-    assert pf(16) == jl.JL_ERR_ARG
+    assert pf(32) == jl.JL_ERR_ARG
+    assert pf(jl.JL_PREFILL_CTA_PAIR | jl.JL_PREFILL_ONE_CTA) == jl.JL_ERR_ARG
     assert pf(SW | PQ) == jl.JL_ERR_ARG
     assert pf(SW | SH) == jl.JL_ERR_ARG
     assert pf(PQ | SH) == jl.JL_ERR_UNSUPPORTED

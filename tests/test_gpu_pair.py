@@ -1,8 +1,10 @@
-"""The two-SM prefill tile kernel (JL_PREFILL_CTA_PAIR: a cluster of two CTAs
-per query tile of four heads, tcgen05 MMAs of M = 256 across both SMs, each
-CTA correcting half of every K tile) against the fp64 oracle, element by
-element, on the shapes it applies to (D = 128, Hq / Hkv a multiple of 4);
-elsewhere the flag must leave the result bit for bit as without it."""
+"""The two prefill tile kernels against the fp64 oracle and against each
+other's selection rules.  The two-SM kernel (a cluster of two CTAs per query
+tile of four heads, tcgen05 MMAs of M = 256 across both SMs, each CTA
+correcting half of every K tile) is forced with JL_PREFILL_CTA_PAIR on the
+shapes it applies to (D = 128, Hq / Hkv a multiple of 4); elsewhere that flag
+must leave the result bit for bit as without it.  The one-CTA kernel is
+forced with JL_PREFILL_ONE_CTA where the default would pick the two-SM one."""
 import numpy as np
 import pytest
 
@@ -11,10 +13,11 @@ import helpers
 pytestmark = pytest.mark.gpu
 
 PAIR = 8
+ONE = 16
 PQ, SW, SH = 1, 2, 4
 
 
-def _case(jl, orc, dev, B, Hq, Hkv, S_new, n_past, L, w, flags, seed, rows=None, D=128):
+def _case(jl, orc, dev, B, Hq, Hkv, S_new, n_past, L, w, flags, seed, rows=None, D=128, kernel=PAIR):
     from zero_shot_rope_02_b300 import inputs
 
     s = n_past + S_new
@@ -22,7 +25,7 @@ def _case(jl, orc, dev, B, Hq, Hkv, S_new, n_past, L, w, flags, seed, rows=None,
     k_t, k_f = helpers.bf16_pair((B, s, Hkv, D), seed, 1)
     v_t, v_f = helpers.bf16_pair((B, s, Hkv, D), seed, 2)
     out, lse = jl.jl_bifocal_prefill_ex(inputs.to_torch_bf16(qb).to(dev), k_t.to(dev), v_t.to(dev), n_past, L, w,
-                                        1e6, flags | PAIR)
+                                        1e6, flags | kernel)
     assert jl.jl_debug_status() == 0
     if rows is None:
         rows = np.arange(S_new)
@@ -69,3 +72,40 @@ def test_pair_flag_is_ignored_where_it_does_not_apply(jl, dev):
         o0, l0 = jl.jl_bifocal_prefill_ex(q, k, v, 0, 200, 150, 1e6, 0)
         o1, l1 = jl.jl_bifocal_prefill_ex(q, k, v, 0, 200, 150, 1e6, PAIR)
         assert torch.equal(o0, o1) and torch.equal(l0, l1), (Hq, Hkv, D)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S_new,n_past,L,w,flags", [
+    (1, 4, 1, 1000, 0, 300, 256, 0),     # grp = 4, g = 4
+    (2, 8, 2, 700, 0, 200, 150, 0),      # ragged, band tiles
+    (1, 4, 1, 300, 700, 100, 200, 0),    # a chunk over a cache
+    (1, 4, 1, 700, 0, 200, 150, PQ),     # per-query g
+    (1, 4, 1, 700, 0, 200, 150, SH),     # query shift
+])
+def test_one_cta_kernel_parity_where_the_pair_is_default(jl, orc, dev, B, Hq, Hkv, S_new, n_past, L, w, flags):
+    _case(jl, orc, dev, B, Hq, Hkv, S_new, n_past, L, w, flags, seed=67, kernel=ONE)
+
+
+def test_one_cta_kernel_at_128k_sampled(jl, orc, dev):
+    """The Qwen3-8B-shaped 128K layer on the one-CTA kernel: one seeded row of
+    every 1024, plus the rule edges."""
+    S, L, w = 131072, 32768, 4096
+    rng = np.random.default_rng(69)
+    rows = set(int(r) for r in helpers.sample_rows(S, L, w, 4, n_random=0))
+    rows.update(int(1024 * b + rng.integers(0, 1024)) for b in range(S // 1024))
+    _case(jl, orc, dev, 1, 32, 8, S, 0, L, w, 0, seed=2, rows=np.array(sorted(rows)), kernel=ONE)
+
+
+def test_default_kernel_choice(jl, dev):
+    """Four heads per kv head at D = 128: with remote keys the default is the
+    two-SM kernel, bit for bit; all exact (g = 1) it is the one-CTA kernel."""
+    import torch
+
+    q_t, _ = helpers.bf16_pair((1, 900, 8, 128), 71, 0)
+    k_t, _ = helpers.bf16_pair((1, 900, 2, 128), 71, 1)
+    v_t, _ = helpers.bf16_pair((1, 900, 2, 128), 71, 2)
+    q, k, v = q_t.to(dev), k_t.to(dev), v_t.to(dev)
+    for L, forced in ((200, PAIR), (1000, ONE)):
+        o0, l0 = jl.jl_bifocal_prefill_ex(q, k, v, 0, L, 150, 1e6, 0)
+        o1, l1 = jl.jl_bifocal_prefill_ex(q, k, v, 0, L, 150, 1e6, forced)
+        assert torch.equal(o0, o1) and torch.equal(l0, l1), (L, forced)
+    assert jl.jl_debug_status() == 0

@@ -14,6 +14,7 @@ _BINDING_NAMES = (
     "jl_bifocal_decode_paged", "jl_bifocal_decode_paged_workspace_size", "jl_rope_cache_write",
     "jl_group_factor_ex", "jl_bifocal_prefill_ex", "jl_bifocal_decode_ex", "JL_VARIANT_PER_QUERY_G",
     "JL_VARIANT_SLIDING", "JL_VARIANT_QUERY_SHIFT", "JL_PREFILL_CTA_PAIR",
+    "JL_PREFILL_ONE_CTA",
 )
 
 __all__ = list(_BINDING_NAMES)

@@ -40,8 +40,10 @@ EXPORTS = (
 JL_VARIANT_PER_QUERY_G = 1
 JL_VARIANT_SLIDING = 2
 JL_VARIANT_QUERY_SHIFT = 4
-# jl_bifocal_prefill_ex: the two-SM (cta_group::2) tile kernel where it applies
+# jl_bifocal_prefill_ex kernel choice: force the two-SM (cta_group::2) tile
+# kernel where it applies, or force the one-CTA kernel (default: automatic)
 JL_PREFILL_CTA_PAIR = 8
+JL_PREFILL_ONE_CTA = 16
 
 
 class JetLongError(RuntimeError):

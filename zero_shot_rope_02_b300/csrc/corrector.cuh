@@ -39,6 +39,9 @@ struct RotConsts {
     alignas(8) float a2c[64];
     alignas(8) float a2s[64];
     alignas(8) float a2ns[64];
+    // the 64 rows another CTA holds in the paired kernel (uniform steps only)
+    alignas(8) float skc[64];
+    alignas(8) float sks[64];
     int uni;  // g divides RPS: every RPS-row step is a
 };
 
@@ -266,20 +269,18 @@ struct Corrector {
         if (uni) {
             if (kt != next_kt || kt % kReanchorTiles == 0) anchor(kt * kCorrTileRows + row0 + n0);
             run_uni(tile);
-            if (ROWS < kCorrTileRows) {
-                // skip the rows the other CTA holds: the chains step 2 RPS rows per a2
+            if constexpr (ROWS < kCorrTileRows) {
+                // skip the 64 rows the other CTA holds: one rotation per chain
+                static_assert(kCorrTileRows - ROWS == 64, "the skip rotation covers 64 rows");
                 jl::f32x2 rcs[4], rsn[4], rns[4];
 #pragma unroll
                 for (int q = 0; q < 4; q++) {
-                    rcs[q] = ld2(rc->a2c + 8 * c + 2 * q);
-                    rsn[q] = ld2(rc->a2s + 8 * c + 2 * q);
-                    rns[q] = ld2(rc->a2ns + 8 * c + 2 * q);
+                    rcs[q] = ld2(rc->skc + 8 * c + 2 * q);
+                    rsn[q] = ld2(rc->sks + 8 * c + 2 * q);
+                    rns[q] = rsn[q] ^ 0x8000000080000000ull;
                 }
-#pragma unroll 1
-                for (int k = 0; k < (kCorrTileRows - ROWS) / (2 * RPS); k++) {
-                    cmul(ec, es, rcs, rsn, rns);
-                    cmul(oc, os, rcs, rsn, rns);
-                }
+                cmul(ec, es, rcs, rsn, rns);
+                cmul(oc, os, rcs, rsn, rns);
             }
             next_kt = kt + 1;
         } else {
@@ -306,6 +307,7 @@ inline void make_rot_consts(const jl::PhaseTable &pt, int D, int g, RotConsts *r
         rc->ans[d] = -rc->as[d];
         rc->bns[d] = -rc->bs[d];
         rc->a2ns[d] = -rc->a2s[d];
+        jl::rotation_host(pt, d, (64 / rps) * (qs - rps), &rc->skc[d], &rc->sks[d]);
     }
 }
 

@@ -709,7 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_4d(sV + sv * C::VHALF, &tv, bar(C::B_VFULL + sv), 64 * (int)rank, hk, vis.kt(v) * kBN, b);
                 issued = v + 1;
                 if (!(ok = wait_bar(bar(C::B_VFULL + sv), (v / NV) & 1, wc))) break;
-                mbar_arrive_cluster(lead(C::B_GO + v % NK));
+                mbar_arrive_peer(lead(C::B_GO + v % NK));
             }
             if (!ok) {
                 for (int v = issued - NV < 0 ? 0 : issued - NV; v < issued; v++)
@@ -884,7 +884,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(n == 0 ? lead(C::B_GO + v % NK) : lead(C::B_PFULL + 1));
+            if (lane == 0) mbar_arrive_peer(n == 0 ? lead(C::B_GO + v % NK) : lead(C::B_PFULL + 1));
         }
         // ------------------------------------------------------------ epilogue
         if (ok) ok = wait_bar_warp_cl(bar(C::B_ODONE + n), (T - 1) & 1, wc);
@@ -944,7 +944,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 !(ok = wait_bar_warp_cl(bar(C::B_KEMPTY + (T - NK) % NK), ((T - NK) / NK) & 1, wc)))
                 break;
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(u == 0 ? lead(C::B_K0READY) : lead(C::B_GO + (u - 1) % NK));
+            if (lane == 0) mbar_arrive_peer(u == 0 ? lead(C::B_K0READY) : lead(C::B_GO + (u - 1) % NK));
         }
     }
 
@@ -1133,7 +1133,7 @@ struct PrefillCall {
     int B, Hq, Hkv, n_cap, D, w;
     int q_rows, lse_stride;  // batch stride of q / out (rows), row stride of lse
     int sliding;
-    int pair;  // the two-SM kernel where it applies (JL_PREFILL_CTA_PAIR)
+    int pair;  // kernel choice: 0 one CTA (JL_PREFILL_ONE_CTA), 1 automatic, 2 two SMs (JL_PREFILL_CTA_PAIR)
     jl::PhaseTable pt;
     float scale_log2;
     cudaStream_t st;
@@ -1180,7 +1180,13 @@ static int prefill_rows(const PrefillCall &c, const void *q, void *out, float *l
     RotConsts rc;
     make_rot_consts(c.pt, D, g, &rc);
     int rc_launch;
-    if (c.pair && D == 128 && p.grp % 4 == 0) {
+    // The two-SM kernel applies at D = 128 with four heads (or a multiple) per
+    // kv head; by default it runs where the launch has remote keys, since it
+    // halves each SM's correction work, and the one-CTA kernel runs the plain
+    // (all-exact) launches, whose handshakes it keeps on one SM.
+    const bool pair_fits = D == 128 && p.grp % 4 == 0;
+    const bool has_remote = g > 1 && !c.sliding && S - 1 >= c.w;
+    if (pair_fits && (c.pair == 2 || (c.pair == 1 && has_remote))) {
         // four heads per kv head or a multiple: a CTA pair per query tile of four heads
         CUtensorMap tk64;
         if (!jl::make_bshd_map(&tk64, c.k, c.B, S, c.n_cap, c.Hkv, D, 64, 64, true)) return JL_ERR_CUDA;
@@ -1232,10 +1238,11 @@ static int prefill_impl(const void *q, const void *k, const void *v, void *out, 
         !(theta > 0.0) || Hq % Hkv != 0)
         return JL_ERR_ARG;
     if (flags & ~(unsigned)(JL_VARIANT_PER_QUERY_G | JL_VARIANT_SLIDING | JL_VARIANT_QUERY_SHIFT |
-                            JL_PREFILL_CTA_PAIR))
+                            JL_PREFILL_CTA_PAIR | JL_PREFILL_ONE_CTA))
         return JL_ERR_ARG;
-    const bool pair = (flags & JL_PREFILL_CTA_PAIR) != 0;
-    flags &= ~(unsigned)JL_PREFILL_CTA_PAIR;
+    if ((flags & JL_PREFILL_CTA_PAIR) && (flags & JL_PREFILL_ONE_CTA)) return JL_ERR_ARG;
+    const int pair = (flags & JL_PREFILL_CTA_PAIR) ? 2 : (flags & JL_PREFILL_ONE_CTA) ? 0 : 1;
+    flags &= ~(unsigned)(JL_PREFILL_CTA_PAIR | JL_PREFILL_ONE_CTA);
     if ((flags & JL_VARIANT_SLIDING) && flags != JL_VARIANT_SLIDING) return JL_ERR_ARG;
     if ((flags & JL_VARIANT_PER_QUERY_G) && (flags & JL_VARIANT_QUERY_SHIFT)) return JL_ERR_UNSUPPORTED;
     if ((long long)n_past + Sq > 0x7fffffffLL) return JL_ERR_OVERFLOW;
@@ -1269,7 +1276,7 @@ static int prefill_impl(const void *q, const void *k, const void *v, void *out, 
     c.q_rows = Sq;
     c.lse_stride = Sq;
     c.sliding = (flags & JL_VARIANT_SLIDING) ? 1 : 0;
-    c.pair = pair ? 1 : 0;
+    c.pair = pair;
     if (!jl::make_phase_table(&c.pt, D, theta)) return JL_ERR_ARG;
     c.scale_log2 = (float)(1.0 / sqrt((double)D) * 1.4426950408889634);
     c.st = (cudaStream_t)stream;

@@ -310,6 +310,19 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// Arrive on an mbarrier given by its cluster-window address with a release at
+// CTA scope only.  For the paired MMA's handshakes: what an arrival publishes
+// (a corrected K half, a P tile in TMEM, a landed V half) lives in the
+// arriving CTA's own shared memory or TMEM and is read there by its own SM's
+// tensor core, after the peer's issuing thread has seen the arrival; a CTA
+// release performs those writes on this SM first.  A cluster-scope release
+// (mbar_arrive_cluster) costs several hundred cycles per handshake on B300
+// and made the paired kernel 20% slower.
+__device__ __forceinline__ void mbar_arrive_peer(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 // try_wait that acquires at cluster scope (arrivals may come from the peer CTA).
 __device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity)
 {
