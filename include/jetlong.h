@@ -268,7 +268,9 @@ size_t jl_bifocal_decode_workspace_size(int B, int Hq, int Hkv, int n, int D);
  * cores (bf16 operands for exact keys, fp16 for corrected ones as in the
  * prefill, fp32 accumulation, P rounded to bf16 for P.V with out normalised
  * by the sum of the rounded P and lse by the fp32 sum); shorter caches and
- * D = 64 use fp32 arithmetic on CUDA cores throughout.
+ * D = 64 use fp32 arithmetic on CUDA cores throughout.  The paged decode at
+ * D = 128 runs on the tensor cores for every length, its sequences shorter
+ * than 256 keys with P split into a high and a low bf16 part for P.V.
  * Kernels exist for GQA group sizes Hq / Hkv in {1, 2, 4, 8}; any other group
  * size returns JL_ERR_UNSUPPORTED (this also holds for the paged and the
  * no-allocation variants).

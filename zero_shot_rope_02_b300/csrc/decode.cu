@@ -612,30 +612,34 @@ constexpr int kTcNS = 3;
 constexpr int kTcThreads = 352;
 constexpr int kTcN = 16;
 constexpr float kTcRescaleThreshold = 8.0f;  // log2 units, as the prefill's lazy offset
-// Shorter caches take the scalar kernel: its fp32 P keeps outputs over a few
-// keys within the stated bounds, where the rounding of P to bf16 for the
-// tensor core is not averaged out.
+// Shorter contiguous caches take the scalar kernel; the paged batch takes this
+// kernel for every length, its shorter sequences with P split into two bf16
+// parts for P.V.
 constexpr int kTcMinKeys = 256;
 
 struct TcCfg {
     static constexpr int D = 128;
     static constexpr int TILE = kTcKeys * D * 2;     // one K or V tile: 32 KB
     static constexpr int REGION = kTcKeys * 64 * 2;  // one 64-column box of it: 16 KB
+    static constexpr int HALF = REGION / 2;          // 64 rows of a box (one paged load): 8 KB
     static constexpr int QBOX = kTcN * 128;          // 16 rows x 64 16-bit values: 2 KB
     static constexpr int OPND = 2 * QBOX;            // a 16 x 128 operand (Q^T or P^T): 4 KB
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = OFF_K + kTcNS * TILE;
     static constexpr int OFF_QE = OFF_V + kTcNS * TILE;  // exact q, bf16
     static constexpr int OFF_QR = OFF_QE + OPND;         // corrected q, fp16
-    static constexpr int OFF_P = OFF_QR + OPND;          // P^T, two buffers
-    static constexpr int OFF_RED = OFF_P + 2 * OPND;     // fp32 [2][4 warps][8 heads] maxima, [4][16] sums
-    static constexpr int OFF_BAR = OFF_RED + (2 * 4 * 8 + 4 * 16) * 4;
+    static constexpr int OFF_P = OFF_QR + OPND;          // P^T high and low parts, two tiles
+    static constexpr int OFF_RED = OFF_P + 4 * OPND;     // fp32 [2][4 warps][8 heads] maxima, [4][16] sums
+    static constexpr int OFF_RC = OFF_RED + (2 * 4 * 8 + 4 * 16) * 4;  // paged: this sequence's RotConsts
+    static constexpr int OFF_BAR = (OFF_RC + (int)sizeof(RotConsts) + 15) / 16 * 16;
     static constexpr int B_KFULL = 0, B_KEMPTY = B_KFULL + kTcNS, B_KREADY = B_KEMPTY + kTcNS,
                          B_VFULL = B_KREADY + kTcNS, B_VEMPTY = B_VFULL + kTcNS, B_SFULL = B_VEMPTY + kTcNS,
                          B_PFULL = B_SFULL + 2, B_ODONE = B_PFULL + 2, B_QREADY = B_ODONE + 1,
-                         B_BANDQK = B_QREADY + 1, B_DRAIN = B_BANDQK + 1, NBAR = B_DRAIN + 1;
-    static constexpr int OFF_TMEM_SLOT = NBAR * 8, OFF_ABORT = OFF_TMEM_SLOT + 4, OFF_LAST = OFF_ABORT + 4;
-    static constexpr int SMEM = OFF_BAR + OFF_LAST + 4 + 1024;  // + alignment slack
+                         B_BANDQK = B_QREADY + 1, B_DRAIN = B_BANDQK + 1, B_VREADY = B_DRAIN + 1,
+                         NBAR = B_VREADY + 1;
+    static constexpr int OFF_TMEM_SLOT = NBAR * 8, OFF_ABORT = OFF_TMEM_SLOT + 4, OFF_LAST = OFF_ABORT + 4,
+                         OFF_PLAN = OFF_LAST + 4;  // paged: 5 ints
+    static constexpr int SMEM = OFF_BAR + OFF_PLAN + 5 * 4 + 1024;  // + alignment slack
     static_assert(SMEM <= 232448, "shared memory budget");
     // the merge's scratch (GRP x 256 weights, then m and l) reuses the K ring
     static_assert(8 * 256 * 4 + 2 * 8 * 4 <= kTcNS * TILE, "merge scratch");
@@ -649,7 +653,7 @@ __device__ __forceinline__ uint32_t tc_opnd_off(int row, int col)
                       (col & 7) * 2);
 }
 
-template <int GRP>
+template <int GRP, bool PAGED>
 __global__ void __launch_bounds__(kTcThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                      const DecodeArgs a, const __grid_constant__ jl::PhaseTable pt,
@@ -671,11 +675,61 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const WaitCtx wc{a.status, abort_flag};
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int hk = blockIdx.y, b = blockIdx.z, split = blockIdx.x;
-    const int n = a.n, g = a.g, ns = a.splits;
-    const int j_begin = split * a.chunk;
-    const int j_end = min(n, j_begin + a.chunk);
+    const int hk = blockIdx.y;
+    // this CTA's sequence b, its split, the sequence's split count ns and
+    // length n, the chunk size, and the split stride of the partial layout
+    int b = blockIdx.z, split = blockIdx.x, ns = a.splits, n = a.n, chunk = a.chunk, g = a.g;
+    const int stride = a.splits;
+    if constexpr (PAGED) {
+        // splits in proportion to the lengths (as the scalar paged kernel),
+        // chunks a multiple of the 128-key tile
+        volatile int *s_plan = reinterpret_cast<volatile int *>(smem + C::OFF_BAR + C::OFF_PLAN);
+        if (tid == 0) {
+            const int n_lim = min(a.max_pages * a.page_size, a.n);
+            long long tot = 0;
+            bool bad = false;
+            for (int q = 0; q < a.B; q++) {
+                const int ls = a.seq_lens[q];
+                bad = bad || ls < 1 || ls > n_lim;
+                tot += min(max(ls, 1), n_lim);
+            }
+            if (bad && blockIdx.x == 0 && hk == 0) jl::record_status(a.status, JL_ERR_GUARD);
+            long long ch = (tot + a.splits - 1) / a.splits;
+            ch = (ch + kTcKeys - 1) / kTcKeys * kTcKeys;
+            int bb = -1, sp = 0, nsb = 0, nb = 0, cum = 0;
+            for (int q = 0; q < a.B; q++) {
+                const int ls = min(max(a.seq_lens[q], 1), n_lim);
+                const int sb = (int)((ls + ch - 1) / ch);
+                if ((int)blockIdx.x < cum + sb) {
+                    bb = q;
+                    sp = (int)blockIdx.x - cum;
+                    nsb = sb;
+                    nb = ls;
+                    break;
+                }
+                cum += sb;
+            }
+            s_plan[0] = bb;
+            s_plan[1] = sp;
+            s_plan[2] = nsb;
+            s_plan[3] = nb;
+            s_plan[4] = (int)ch;
+        }
+        __syncthreads();
+        b = s_plan[0];
+        if (b < 0) return;  // past the last sequence's splits: no work (nothing allocated yet)
+        split = s_plan[1];
+        ns = s_plan[2];
+        n = s_plan[3];
+        chunk = s_plan[4];
+        g = (n <= a.L) ? 1 : (n - 1) / a.L + 1;
+    }
+    const int j_begin = split * chunk;
+    const int j_end = min(n, j_begin + chunk);
     const int T = (j_end - j_begin + kTcKeys - 1) / kTcKeys;
+    // Over fewer than kTcMinKeys keys the rounding of P to bf16 is not averaged
+    // out: P.V then takes P as a high and a low bf16 part (P to ~2^-17).
+    const bool split_p = n < kTcMinKeys;
     const int j_split = (g > 1) ? max(0, n - a.w) : 0;  // keys below are remote
     const bool any_remote = j_begin < j_split;
     // tile classes: 0 exact, 1 remote, 2 crossed by the window edge
@@ -700,6 +754,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_init(bar(C::B_QREADY), 4);
         mbar_init(bar(C::B_BANDQK), 1);
         mbar_init(bar(C::B_DRAIN), 1);
+        mbar_init(bar(C::B_VREADY), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -727,16 +782,57 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int v = 0; v < T; v++) {
                 const int s = v % NS;
                 if (!(ok = wait_bar(bar(b_empty + s), ((v / NS) & 1) ^ 1, wc))) break;
-                mbar_arrive_expect_tx(bar(b_full + s), C::TILE);
+                const int row0 = j_begin + v * kTcKeys;
+                if constexpr (PAGED) {
+                    // two 64-row halves, each from its own page (page sizes are
+                    // multiples of 64); a half wholly past the sequence loads nothing.
+                    // A page id outside the pool reads zeros (TMA bounds) and is reported.
+                    const int halves = (j_end - row0 > 64) ? 2 : 1;
+                    mbar_arrive_expect_tx(bar(b_full + s), halves * 2 * C::HALF);
+                    for (int hh = 0; hh < halves; hh++) {
+                        const int row = row0 + 64 * hh;
+                        const int page = a.block_table[(size_t)b * a.max_pages + row / a.page_size];
+                        if ((unsigned)page >= (unsigned)a.num_pages) jl::record_status(a.status, JL_ERR_GUARD);
 #pragma unroll
-                for (int r = 0; r < 2; r++)
-                    tma_load_4d(ring + s * C::TILE + r * C::REGION, m, bar(b_full + s), r * 64, hk,
-                                j_begin + v * kTcKeys, b);
+                        for (int r = 0; r < 2; r++)
+                            tma_load_4d(ring + s * C::TILE + r * C::REGION + hh * C::HALF, m, bar(b_full + s),
+                                        r * 64, hk, row % a.page_size, page);
+                    }
+                } else {
+                    mbar_arrive_expect_tx(bar(b_full + s), C::TILE);
+#pragma unroll
+                    for (int r = 0; r < 2; r++)
+                        tma_load_4d(ring + s * C::TILE + r * C::REGION, m, bar(b_full + s), r * 64, hk, row0, b);
+                }
                 issued = v + 1;
             }
             if (!ok)
                 for (int v = issued - NS < 0 ? 0 : issued - NS; v < issued; v++)
                     drain_bar(bar(b_full + v % NS), (v / NS) & 1);
+        }
+        if constexpr (PAGED) {
+            if (warp == 9) {
+                // The last tile's V rows past the sequence hold whatever the pool
+                // (or an earlier tile) left there: zero them before its P.V, where
+                // 0 * NaN would still poison O.  The issuer waits on VREADY for it.
+                __syncwarp();
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                const int v = T - 1, s = v % NS;
+                if (ok) ok = wait_bar_warp(bar(C::B_VFULL + s), (v / NS) & 1, wc);
+                if (ok) {
+                    const int valid = j_end - (j_begin + v * kTcKeys);  // 1..128 rows hold keys
+                    const int nz = (kTcKeys - valid) * 8;              // 16-byte chunks per box
+                    for (int e = lane; e < 2 * nz; e += 32) {
+                        const int r = e / nz, rem = e % nz;
+                        *reinterpret_cast<uint4 *>(smem + C::OFF_V + s * C::TILE + r * C::REGION +
+                                                   (valid + rem / 8) * 128 + (rem % 8) * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(C::B_VREADY));
+                }
+            }
         }
     } else if (warp == 10) {
         // ------------------------------------------------------------ MMA issuer
@@ -778,15 +874,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (v + 1 < T && !(ok = qk_tile(v + 1))) break;
                 const int s = v % NS;
                 if (!(ok = wait_bar(bar(C::B_PFULL + (v & 1)), (v >> 1) & 1, wc))) break;
-                if (!(ok = wait_bar(bar(C::B_VFULL + s), (v / NS) & 1, wc))) break;
+                // the paged batch's last tile: V with its rows past the sequence zeroed
+                const bool vready = PAGED && v == T - 1;
+                if (!(ok = wait_bar(bar(vready ? C::B_VREADY : C::B_VFULL + s), vready ? 0u : (v / NS) & 1, wc)))
+                    break;
                 tc_fence_after();
                 const uint64_t dv = sdesc_sw128(sV + s * C::TILE, C::REGION, 1024);
-                const uint64_t dp = sdesc_sw128(sP + (v & 1) * C::OPND, 16, 1024);
+                // P.V on the rounded P, or P = P_hi + P_lo (bf16 each) over few keys:
+                // O^T += V^T P_hi^T (+ V^T P_lo^T)
+                for (int part = 0; part < (split_p ? 2 : 1); part++) {
+                    const uint64_t dp = sdesc_sw128(sP + (2 * (v & 1) + part) * C::OPND, 16, 1024);
 #pragma unroll
-                for (int k = 0; k < kTcKeys / 16; k++)
-                    mma_f16_ss(tmem + 64u, dv + (uint64_t)((k * 2048) >> 4),
-                               dp + (uint64_t)(((k >> 2) * C::QBOX + (k & 3) * 32) >> 4), idPV,
-                               (v > 0 || k > 0) ? 1u : 0u);
+                    for (int k = 0; k < kTcKeys / 16; k++)
+                        mma_f16_ss(tmem + 64u, dv + (uint64_t)((k * 2048) >> 4),
+                                   dp + (uint64_t)(((k >> 2) * C::QBOX + (k & 3) * 32) >> 4), idPV,
+                                   (v > 0 || part > 0 || k > 0) ? 1u : 0u);
+                }
                 mma_commit(bar(C::B_VEMPTY + s));
                 mma_commit(bar(C::B_ODONE));
             }
@@ -803,7 +906,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // (the edge tile after its exact QK has read it) and arrives on KREADY.
         const int t = tid - 128;
         Corrector<D> cor;
-        if (any_remote) cor.init(t, g, pt, rc);
+        if constexpr (PAGED) {
+            // this sequence's g sets the step rotations: build them in shared
+            // memory from the exact phase (pairs d = t, 64 threads), as the host
+            // does for the contiguous cache
+            RotConsts *src = reinterpret_cast<RotConsts *>(smem + C::OFF_RC);
+            if (any_remote && t < D / 2) {
+                const int rps = 128 / (D / 16);
+                const int qs = rps / g;
+                const int offs[4] = {qs - rps, qs + 1 - rps, 2 * (qs - rps), (64 / rps) * (qs - rps)};
+                float cs[4], sn[4];
+#pragma unroll
+                for (int u = 0; u < 4; u++) jl::phase_sincos(offs[u], pt.f[t], &sn[u], &cs[u]);
+                src->ac[t] = cs[0];
+                src->as[t] = sn[0];
+                src->ans[t] = -sn[0];
+                src->bc[t] = cs[1];
+                src->bs[t] = sn[1];
+                src->bns[t] = -sn[1];
+                src->a2c[t] = cs[2];
+                src->a2s[t] = sn[2];
+                src->a2ns[t] = -sn[2];
+                src->skc[t] = cs[3];
+                src->sks[t] = sn[3];
+                if (t == 0) src->uni = (rps % g == 0) ? 1 : 0;
+            }
+            asm volatile("bar.sync 2, 128;" ::: "memory");  // the correction warps only
+            if (any_remote) cor.init(t, g, pt, *src);
+        } else {
+            if (any_remote) cor.init(t, g, pt, rc);
+        }
         for (int v = 0; ok && v < T; v++) {
             const int s = v % NS, cls = tclass(v);
             if (!(ok = wait_bar_warp(bar(C::B_KFULL + s), (v / NS) & 1, wc))) break;
@@ -937,17 +1069,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tmem_st16(tmem + lane_base + 64u, o);
                 tmem_st_wait();
             }
-            // P^T(v): its buffer was last read by the P.V of tile v-2, which
-            // completed before QK(v) (one issuing thread, in-order pipe)
-            uint8_t *pbuf = smem + C::OFF_P + (v & 1) * C::OPND;
+            // P^T(v), rounded to bf16 (and over few keys its low part too).
+            // lr sums the P that P.V multiplies and normalises out; l, the fp32
+            // sum, gives lse.  The buffers were last read by the P.V of tile
+            // v-2, which completed before QK(v) (one issuing thread, in-order pipe).
+            uint8_t *pbuf = smem + C::OFF_P + 2 * (v & 1) * C::OPND;
 #pragma unroll
             for (int h = 0; h < GRP; h++) {
                 const float off = (m_run[h] == -INFINITY) ? 0.f : m_run[h];
                 const float pv = exp2f(x[h] - off);
-                const __nv_bfloat16 pb = __float2bfloat16_rn(pv);
+                const __nv_bfloat16 ph = __float2bfloat16_rn(pv);
+                const float phf = __bfloat162float(ph);
                 l_run[h] += pv;
-                lr_run[h] += __bfloat162float(pb);
-                *reinterpret_cast<__nv_bfloat16 *>(pbuf + tc_opnd_off(h, t)) = pb;
+                *reinterpret_cast<__nv_bfloat16 *>(pbuf + tc_opnd_off(h, t)) = ph;
+                if (split_p) {
+                    const __nv_bfloat16 pl = __float2bfloat16_rn(pv - phf);
+                    lr_run[h] += phf + __bfloat162float(pl);
+                    *reinterpret_cast<__nv_bfloat16 *>(pbuf + C::OPND + tc_opnd_off(h, t)) = pl;
+                } else {
+                    lr_run[h] += phf;
+                }
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -1002,14 +1143,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (t == h) a.lse[hq0 + h] = (m_run[h] + log2f(l_run[h])) * kLn2;
                 }
             } else {
-                // out is normalised by the sum of the rounded P that P.V used,
-                // lse by the fp32 sum; the merge weighs splits by l
 #pragma unroll
                 for (int h = 0; h < GRP; h++) {
-                    a.part_o[((hq0 + h) * ns + split) * D + t] = o_h[h] * (l_run[h] / lr_run[h]);
+                    // the merge weighs splits by l: o scaled to the fp32 sum
+                    a.part_o[((hq0 + h) * stride + split) * D + t] = o_h[h] * (l_run[h] / lr_run[h]);
                     if (t == h) {
-                        a.part_ml[((hq0 + h) * ns + split) * 2 + 0] = m_run[h];
-                        a.part_ml[((hq0 + h) * ns + split) * 2 + 1] = l_run[h];
+                        a.part_ml[((hq0 + h) * stride + split) * 2 + 0] = m_run[h];
+                        a.part_ml[((hq0 + h) * stride + split) * 2 + 1] = l_run[h];
                     }
                 }
             }
@@ -1023,7 +1163,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // the K ring is free now: the merge's scratch
     if (warp < 4 && ok && ns > 1) {
         float *mw = reinterpret_cast<float *>(smem + C::OFF_K);
-        ticket_and_merge<D, GRP>(a, b, hk, ns, ns, mw, mw + GRP * 256, mw + GRP * 256 + 8, s_last);
+        ticket_and_merge<D, GRP>(a, b, hk, ns, stride, mw, mw + GRP * 256, mw + GRP * 256 + 8, s_last);
     }
 }
 
@@ -1127,11 +1267,11 @@ Plan make_tc_plan(int B, int Hkv, int n, int splits_cap)
     return Plan{(int)splits, (int)chunk, splits_cap};
 }
 
-template <int GRP>
+template <int GRP, bool PAGED>
 int launch_tc(const DecodeArgs &a, int B, const CUtensorMap &tk, const CUtensorMap &tv,
               const jl::PhaseTable &pt, const RotConsts &rc, cudaStream_t st)
 {
-    auto kern = decode_tc_kernel<GRP>;
+    auto kern = decode_tc_kernel<GRP, PAGED>;
     static bool attr_set[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return jl::cuda_status(cudaGetLastError());
@@ -1140,9 +1280,23 @@ int launch_tc(const DecodeArgs &a, int B, const CUtensorMap &tk, const CUtensorM
         if (e != cudaSuccess) return jl::cuda_status(e);
         attr_set[dev] = true;
     }
-    dim3 grid(a.splits, a.Hkv, B);
+    // paged: a.splits CTAs per kv head shared by the batch in proportion to the
+    // lengths, plus one per sequence for rounding; the surplus exits at once
+    dim3 grid(PAGED ? a.splits + B : a.splits, a.Hkv, PAGED ? 1 : B);
     kern<<<grid, kTcThreads, TcCfg::SMEM, st>>>(tk, tv, a, pt, rc);
     return jl::cuda_status(cudaGetLastError());
+}
+
+template <bool PAGED>
+int dispatch_tc(int grp, const DecodeArgs &a, int B, const CUtensorMap &tk, const CUtensorMap &tv,
+                const jl::PhaseTable &pt, const RotConsts &rc, cudaStream_t st)
+{
+    switch (grp) {
+    case 1: return launch_tc<1, PAGED>(a, B, tk, tv, pt, rc, st);
+    case 2: return launch_tc<2, PAGED>(a, B, tk, tv, pt, rc, st);
+    case 4: return launch_tc<4, PAGED>(a, B, tk, tv, pt, rc, st);
+    default: return launch_tc<8, PAGED>(a, B, tk, tv, pt, rc, st);
+    }
 }
 
 template <int D, int GRP, bool PAGED>
@@ -1285,12 +1439,7 @@ static int decode_impl(const void *q, const void *k_cache, const void *v_cache, 
         if (!jl::make_bshd_map(&tk, k_cache, B, n, n_cap, Hkv, D, 64, kTcKeys, true) ||
             !jl::make_bshd_map(&tv, v_cache, B, n, n_cap, Hkv, D, 64, kTcKeys, true))
             return JL_ERR_CUDA;
-        switch (Hq / Hkv) {
-        case 1: return launch_tc<1>(a, B, tk, tv, *pt, *rcs, (cudaStream_t)stream);
-        case 2: return launch_tc<2>(a, B, tk, tv, *pt, *rcs, (cudaStream_t)stream);
-        case 4: return launch_tc<4>(a, B, tk, tv, *pt, *rcs, (cudaStream_t)stream);
-        default: return launch_tc<8>(a, B, tk, tv, *pt, *rcs, (cudaStream_t)stream);
-        }
+        return dispatch_tc<false>(Hq / Hkv, a, B, tk, tv, *pt, *rcs, (cudaStream_t)stream);
     }
     // only rows [0, n) are mapped: the block that holds key n-1 reads zeros past
     // it, never the cache's unused capacity (0 * NaN would poison P.V)
@@ -1368,8 +1517,21 @@ extern "C" int jl_bifocal_decode_paged(const void *q, const void *k_pages, const
     a.B = B;
     const jl::PhaseTable *pt = nullptr;
     const DecRot *rot = nullptr;
-    if (!host_tables(D, theta, 1, &pt, &rot)) return JL_ERR_ARG;  // per-sequence g on the device
+    const RotConsts *rcs = nullptr;
+    if (!host_tables(D, theta, 1, &pt, &rot, &rcs)) return JL_ERR_ARG;  // per-sequence g on the device
     CUtensorMap tk, tv;
+    if (D == 128) {
+        // the tensor-core kernel: one wave of CTAs, (budget + B) per kv head at
+        // most, 64-row halves of its 128-key tiles loaded page by page
+        long long budget = 148LL / Hkv - B;
+        if (budget < 1) budget = 1;
+        if (budget > a.splits) budget = a.splits;  // the workspace's split capacity
+        a.splits = (int)budget;
+        if (!jl::make_bshd_map(&tk, k_pages, num_pages, page_size, page_size, Hkv, D, 64, 64, true) ||
+            !jl::make_bshd_map(&tv, v_pages, num_pages, page_size, page_size, Hkv, D, 64, 64, true))
+            return JL_ERR_CUDA;
+        return dispatch_tc<true>(Hq / Hkv, a, B, tk, tv, *pt, *rcs, (cudaStream_t)stream);
+    }
     // the pool as num_pages units of page_size rows: a page id outside it reads zeros
     if (!jl::make_bshd_map(&tk, k_pages, num_pages, page_size, page_size, Hkv, D, D, kKB, false) ||
         !jl::make_bshd_map(&tv, v_pages, num_pages, page_size, page_size, Hkv, D, D, kKB, false))
