@@ -107,8 +107,7 @@ struct Corrector {
 #pragma unroll
         for (int q = 0; q < 4; q++) {
             const jl::f32x2 x = jl::bf16x2_to_f2(a[q]), y = jl::bf16x2_to_f2(b[q]);
-            const jl::f32x2 ny = y ^ 0x8000000080000000ull;
-            ao[q] = jl::f2_to_f16x2(jl::fma2(x, zc[q], jl::mul2(ny, zs[q])));
+            ao[q] = jl::f2_to_f16x2(jl::sub2(jl::mul2(x, zc[q]), jl::mul2(y, zs[q])));
             bo[q] = jl::f2_to_f16x2(jl::fma2(y, zc[q], jl::mul2(x, zs[q])));
         }
     }
