@@ -154,6 +154,30 @@ def test_decode_tensor_core_path(jl, orc, dev, B, Hq, Hkv, n, n_cap, L, w):
     _decode_case(jl, orc, dev, B, Hq, Hkv, n, n_cap, 128, L, w, 1e6, seed=11)
 
 
+def test_decode_tensor_core_rescales(jl, orc, dev):
+    """The tensor-core decode's running offset under scores that jump by
+    hundreds of log2 units from tile to tile inside one split (keys doubled
+    every 256 positions from 1000 on, queries x 2^3; six tiles per split):
+    O must be rescaled in TMEM between its P.V steps.  L >= n: every tile
+    exact, bf16 operands (as the prefill's jumping-scores test)."""
+    import torch
+
+    B, Hq, Hkv, n, D, L, w = 4, 8, 8, 3000, 128, 4096, 256
+    q_t, q_f = helpers.bf16_pair((B, Hq, D), 17, 3, scale=8.0)
+    k_t, k_f = helpers.bf16_pair((B, n, Hkv, D), 17, 4)
+    v_t, v_f = helpers.bf16_pair((B, n, Hkv, D), 17, 5, scale=0.25)
+    for j in range(1000, n, 256):
+        k_t[:, j:] *= 2.0
+        k_f[:, j:] *= 2.0
+    out, lse = jl.jl_bifocal_decode(_cuda(q_t, dev), _cuda(k_t, dev), _cuda(v_t, dev), n, L, w, 1e6)
+    assert jl.jl_debug_status() == 0
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    ref_o, ref_l = orc.bifocal_decode(q_f[:, None], k_f, v_f, L, w, 1e6)
+    assert float(np.max(ref_l)) > 500.0  # the jumps are really there
+    helpers.compare(helpers.bf16_to_f64(out), lse.cpu().numpy(), ref_o[:, 0], ref_l[:, :, 0],
+                    "decode with jumping scores")
+
+
 @pytest.mark.parametrize("n", [8192, 32768, 131072])
 def test_decode_parity_benchmark_sizes(jl, orc, dev, n):
     """Single-batch decode, Hq=32, Hkv=8, D=128, L=32768, w=4096, theta=1e6 (g = 1, 1, 4)."""

@@ -634,7 +634,7 @@ struct TcCfg {
     static constexpr int OFF_BAR = (OFF_RC + (int)sizeof(RotConsts) + 15) / 16 * 16;
     static constexpr int B_KFULL = 0, B_KEMPTY = B_KFULL + kTcNS, B_KREADY = B_KEMPTY + kTcNS,
                          B_VFULL = B_KREADY + kTcNS, B_VEMPTY = B_VFULL + kTcNS, B_SFULL = B_VEMPTY + kTcNS,
-                         B_PFULL = B_SFULL + 2, B_ODONE = B_PFULL + 2, B_QREADY = B_ODONE + 1,
+                         B_PFULL = B_SFULL + 2, B_ODONE = B_PFULL + 2, B_QREADY = B_ODONE + 2,
                          B_BANDQK = B_QREADY + 1, B_DRAIN = B_BANDQK + 1, B_VREADY = B_DRAIN + 1,
                          NBAR = B_VREADY + 1;
     static constexpr int OFF_TMEM_SLOT = NBAR * 8, OFF_ABORT = OFF_TMEM_SLOT + 4, OFF_LAST = OFF_ABORT + 4,
@@ -751,6 +751,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(bar(C::B_PFULL + s), 4);  // one per softmax warp
         }
         mbar_init(bar(C::B_ODONE), 1);
+        mbar_init(bar(C::B_ODONE + 1), 1);
         mbar_init(bar(C::B_QREADY), 4);
         mbar_init(bar(C::B_BANDQK), 1);
         mbar_init(bar(C::B_DRAIN), 1);
@@ -891,7 +892,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                    (v > 0 || part > 0 || k > 0) ? 1u : 0u);
                 }
                 mma_commit(bar(C::B_VEMPTY + s));
-                mma_commit(bar(C::B_ODONE));
+                mma_commit(bar(C::B_ODONE + (v & 1)));
             }
             if (!ok) {
                 // no MMA may still run when TMEM is released
@@ -1056,9 +1057,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             if (moved && v > 0) {
                 // O^T holds P.V of tiles < v once the P.V of tile v-1 completed
-                // (SFULL(v) implies P.V(v-2) complete, so ODONE is at most
-                // one phase behind and the parity wait is unambiguous)
-                const bool done = wait_bar_warp(bar(C::B_ODONE), (v - 1) & 1, wc);
+                const bool done = wait_bar_warp(bar(C::B_ODONE + ((v - 1) & 1)), ((v - 1) >> 1) & 1, wc);
                 if (!(ok = compute_sync_and(done))) break;
                 tc_fence_after();
                 uint32_t o[16];
@@ -1096,12 +1095,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (lane == 0) mbar_arrive(bar(C::B_PFULL + (v & 1)));
         }
         // ------------------------------------------------------------ epilogue (TMEM part)
-        // The P.V of the last two tiles may both be in flight here (QK(T-1)
-        // was issued before P.V(T-2)), so ODONE can be two phases behind and
-        // a parity wait on the last phase alone would pass on the older one:
-        // wait for tile T-2's phase first.
-        if (ok && T >= 2) ok = compute_sync_and(wait_bar_warp(bar(C::B_ODONE), (T - 2) & 1, wc));
-        if (ok) ok = compute_sync_and(wait_bar_warp(bar(C::B_ODONE), (T - 1) & 1, wc));
+        // P.V(v) completes a phase of ODONE[v % 2].  With QK(v+1) issued before
+        // P.V(v), the P.V of the last two tiles may both be in flight here, and
+        // on one barrier no parity wait would be right (the last phase's parity
+        // also names the one before the previous); on ODONE[(T-1) % 2] the
+        // phase of P.V(T-1) is at most one behind (SFULL(T-1) implied P.V(T-3)
+        // complete), and its completion implies P.V(T-2)'s (one issuing
+        // thread, in-order pipe).  The rescale's wait above is unambiguous the
+        // same way.
+        if (ok) ok = compute_sync_and(wait_bar_warp(bar(C::B_ODONE + ((T - 1) & 1)), ((T - 1) >> 1) & 1, wc));
         float o_h[GRP];
         if (ok) {
             tc_fence_after();
