@@ -69,6 +69,7 @@ struct DecodeArgs {
     const int *seq_lens;     // [B]
     const int *block_table;  // [B, max_pages]
     int page_size, max_pages, num_pages, L, B;
+    int part_stride;         // tensor-core paged decode: splits per (batch, head) in the partial layout
 };
 
 // Named barrier over the compute warps only (the producer warp never joins).
@@ -679,23 +680,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // this CTA's sequence b, its split, the sequence's split count ns and
     // length n, the chunk size, and the split stride of the partial layout
     int b = blockIdx.z, split = blockIdx.x, ns = a.splits, n = a.n, chunk = a.chunk, g = a.g;
-    const int stride = a.splits;
+    const int stride = PAGED ? a.part_stride : a.splits;
     if constexpr (PAGED) {
-        // splits in proportion to the lengths (as the scalar paged kernel),
-        // chunks a multiple of the 128-key tile
+        // Splits in proportion to the lengths: the smallest chunk (a multiple
+        // of the 128-key tile) for which the batch needs at most gridDim.x
+        // CTAs per kv head, so one wave serves every sequence.
         volatile int *s_plan = reinterpret_cast<volatile int *>(smem + C::OFF_BAR + C::OFF_PLAN);
         if (tid == 0) {
             const int n_lim = min(a.max_pages * a.page_size, a.n);
-            long long tot = 0;
             bool bad = false;
             for (int q = 0; q < a.B; q++) {
                 const int ls = a.seq_lens[q];
                 bad = bad || ls < 1 || ls > n_lim;
-                tot += min(max(ls, 1), n_lim);
             }
             if (bad && blockIdx.x == 0 && hk == 0) jl::record_status(a.status, JL_ERR_GUARD);
-            long long ch = (tot + a.splits - 1) / a.splits;
-            ch = (ch + kTcKeys - 1) / kTcKeys * kTcKeys;
+            auto need = [&](long long ch) {
+                long long cnt = 0;
+                for (int q = 0; q < a.B; q++) cnt += (min(max(a.seq_lens[q], 1), n_lim) + ch - 1) / ch;
+                return cnt;
+            };
+            // need(ch) is non-increasing in ch; at one tile-rounded chunk of the
+            // longest length it is B <= gridDim.x
+            long long lo = 1, hi = ((long long)n_lim + kTcKeys - 1) / kTcKeys;
+            while (lo < hi) {
+                const long long mid = (lo + hi) >> 1;
+                if (need(mid * kTcKeys) <= (long long)gridDim.x) hi = mid;
+                else lo = mid + 1;
+            }
+            const long long ch = lo * kTcKeys;
             int bb = -1, sp = 0, nsb = 0, nb = 0, cum = 0;
             for (int q = 0; q < a.B; q++) {
                 const int ls = min(max(a.seq_lens[q], 1), n_lim);
@@ -1282,9 +1294,9 @@ int launch_tc(const DecodeArgs &a, int B, const CUtensorMap &tk, const CUtensorM
         if (e != cudaSuccess) return jl::cuda_status(e);
         attr_set[dev] = true;
     }
-    // paged: a.splits CTAs per kv head shared by the batch in proportion to the
-    // lengths, plus one per sequence for rounding; the surplus exits at once
-    dim3 grid(PAGED ? a.splits + B : a.splits, a.Hkv, PAGED ? 1 : B);
+    // paged: a.splits CTAs per kv head, shared out by the device in proportion
+    // to the lengths (at most that many are needed; the surplus exits at once)
+    dim3 grid(a.splits, a.Hkv, PAGED ? 1 : B);
     kern<<<grid, kTcThreads, TcCfg::SMEM, st>>>(tk, tv, a, pt, rc);
     return jl::cuda_status(cudaGetLastError());
 }
@@ -1523,12 +1535,16 @@ extern "C" int jl_bifocal_decode_paged(const void *q, const void *k_pages, const
     if (!host_tables(D, theta, 1, &pt, &rot, &rcs)) return JL_ERR_ARG;  // per-sequence g on the device
     CUtensorMap tk, tv;
     if (D == 128) {
-        // the tensor-core kernel: one wave of CTAs, (budget + B) per kv head at
-        // most, 64-row halves of its 128-key tiles loaded page by page
-        long long budget = 148LL / Hkv - B;
-        if (budget < 1) budget = 1;
-        if (budget > a.splits) budget = a.splits;  // the workspace's split capacity
-        a.splits = (int)budget;
+        // the tensor-core kernel: one wave of CTAs (148 / Hkv per kv head, at
+        // least one per sequence), 64-row halves of its 128-key tiles loaded
+        // page by page.  The partial layout's split stride stays within the
+        // workspace's capacity: past it every sequence has one split.
+        long long per_head = 148LL / Hkv;
+        if (per_head > a.splits) per_head = a.splits;  // the workspace's split capacity
+        if (per_head < 1) per_head = 1;
+        const long long grid_x = per_head > B ? per_head : B;
+        a.part_stride = (int)(grid_x < a.splits ? grid_x : a.splits);
+        a.splits = (int)grid_x;
         if (!jl::make_bshd_map(&tk, k_pages, num_pages, page_size, page_size, Hkv, D, 64, 64, true) ||
             !jl::make_bshd_map(&tv, v_pages, num_pages, page_size, page_size, Hkv, D, 64, 64, true))
             return JL_ERR_CUDA;
