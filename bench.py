@@ -38,7 +38,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one 128K bifocal prefill launch, from the ncu
 # counters of a one-launch capture, valid only for the prefill sources they
 # were measured on (first 16 hex digits of the sha256 of their concatenation).
-PREFILL_TRAFFIC = {"sha256_16": "c2746804e3d0db3b", "bytes": 3.5508e9 + 1.0577e9}
+PREFILL_TRAFFIC = {"sha256_16": "28f23a7603d4d8e8", "bytes": 3.5630e9 + 1.0578e9}
 PREFILL_SOURCES = ("prefill.cu", "corrector.cuh", "sm100_ptx.cuh", "jl_common.cuh", "tile_class.cuh")
 
 

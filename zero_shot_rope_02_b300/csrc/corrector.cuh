@@ -214,14 +214,15 @@ struct Corrector {
             jm += rs;
             const bool carry = jm >= g;
             if (carry) jm -= g;
-            jl::f32x2 rcs[4], rsn[4], rns[4];
 #pragma unroll
             for (int q = 0; q < 4; q++) {
-                rcs[q] = carry ? bc2[q] : ac2[q];
-                rsn[q] = carry ? bs2[q] : as2[q];
-                rns[q] = rsn[q] ^ 0x8000000080000000ull;
+                const jl::f32x2 rc2 = carry ? bc2[q] : ac2[q];
+                const jl::f32x2 rs2 = carry ? bs2[q] : as2[q];
+                const jl::f32x2 nc = jl::sub2(jl::mul2(ec[q], rc2), jl::mul2(es[q], rs2));
+                const jl::f32x2 ns = jl::fma2(es[q], rc2, jl::mul2(ec[q], rs2));
+                ec[q] = nc;
+                es[q] = ns;
             }
-            cmul(ec, es, rcs, rsn, rns);
         };
 #pragma unroll 1
         for (int k = 0; k < STEPS; k++) {
