@@ -681,6 +681,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // length n, the chunk size, and the split stride of the partial layout
     int b = blockIdx.z, split = blockIdx.x, ns = a.splits, n = a.n, chunk = a.chunk, g = a.g;
     const int stride = PAGED ? a.part_stride : a.splits;
+    // Programmatic dependent launch: let the next kernel of the stream start
+    // its launch now (every CTA of this grid is resident once all have
+    // passed here), and read nothing another kernel may still write before
+    // the previous one completed.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if constexpr (PAGED) asm volatile("griddepcontrol.wait;" ::: "memory");
     if constexpr (PAGED) {
         // Splits in proportion to the lengths: the smallest chunk (a multiple
         // of the 128-key tile) for which the batch needs at most gridDim.x
@@ -779,6 +785,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    if constexpr (!PAGED) asm volatile("griddepcontrol.wait;" ::: "memory");
     const size_t hq0 = (size_t)b * a.Hq + (size_t)hk * GRP;
     bool ok = true;
     float m_run[GRP], l_run[GRP], lr_run[GRP];  // softmax state (warps 0-3)
@@ -1296,9 +1303,18 @@ int launch_tc(const DecodeArgs &a, int B, const CUtensorMap &tk, const CUtensorM
     }
     // paged: a.splits CTAs per kv head, shared out by the device in proportion
     // to the lengths (at most that many are needed; the surplus exits at once)
-    dim3 grid(a.splits, a.Hkv, PAGED ? 1 : B);
-    kern<<<grid, kTcThreads, TcCfg::SMEM, st>>>(tk, tv, a, pt, rc);
-    return jl::cuda_status(cudaGetLastError());
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(a.splits, a.Hkv, PAGED ? 1 : B);
+    cfg.blockDim = dim3(kTcThreads, 1, 1);
+    cfg.dynamicSmemBytes = TcCfg::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return jl::cuda_status(cudaLaunchKernelEx(&cfg, kern, tk, tv, a, pt, rc));
 }
 
 template <bool PAGED>
